@@ -1,0 +1,11 @@
+"""Float64 CPU oracle (test infrastructure only; never part of the product path)."""
+from .verify_ref import (  # noqa: F401
+    bf16_bits_to_f64,
+    gather_latent_rows,
+    ref_attention_partials,
+    ref_greedy_verify,
+    ref_lse_combine,
+    ref_verify_attention,
+    ref_verify_step,
+    sigmoid,
+)

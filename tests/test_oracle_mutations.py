@@ -1,0 +1,152 @@
+"""Plant a mistake in (a copy of) the oracle and check that some pin fails.
+
+This shows the pins are strong enough to catch the plausible slips: an
+off-by-one bound, a dropped softmax scale, a flipped gate sign, a wrong
+token -> request mapping, a base-2 LSE, the last index on argmax ties, a draft
+compared with the wrong target position, a wrong trim, an unnormalised merge
+weight and a NaN instead of the (-inf, 0) identity.  Mutations live on the CPU
+and only ever in a private copy of the oracle module.
+"""
+import importlib.util
+import sys
+
+import numpy as np
+import pytest
+
+import pins
+
+
+def _fresh_oracle():
+    spec = importlib.util.find_spec("oracle.verify_ref")
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules["_oracle_mutant"] = mod
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _mut_bound_off_by_one(m):
+    orig = m.ref_verify_attention
+
+    def f(q, kv, bt, b, g, qpr, scale):
+        # each token also sees the position right after its own
+        b = np.asarray(b).copy()
+        for t in range(b.shape[0]):
+            cap = int(np.sum(np.asarray(bt[t // qpr]) >= 0)) * kv.shape[1]
+            if b[t] > 0:
+                b[t] = min(b[t] + 1, cap)
+        return orig(q, kv, bt, b, g, qpr, scale)
+    m.ref_verify_attention = f
+
+
+def _mut_no_scale(m):
+    orig = m.ref_verify_attention
+    m.ref_verify_attention = lambda q, kv, bt, b, g, qpr, scale: orig(q, kv, bt, b, g, qpr, 1.0)
+
+
+def _mut_gate_sign(m):
+    orig = m.sigmoid
+    m.sigmoid = lambda x: orig(-np.asarray(x, dtype=np.float64))
+
+
+def _mut_token_mapping(m):
+    orig = m.ref_verify_attention
+
+    def f(q, kv, bt, b, g, qpr, scale):
+        # tokens interleaved across requests instead of request-major
+        T = np.asarray(b).shape[0]
+        R = max(1, T // qpr)
+        order = np.array([(t % R) * qpr + t // R for t in range(T)])
+        out, lse = orig(np.asarray(q)[order], kv, bt, np.asarray(b)[order], np.asarray(g)[order], qpr, scale)
+        inv = np.argsort(order)
+        return out[inv], lse[inv]
+    m.ref_verify_attention = f
+
+
+def _mut_lse_log2(m):
+    orig = m._softmax_stats
+
+    def f(s, rows):
+        lse, o = orig(s, rows)
+        return lse / np.log(2.0), o
+    m._softmax_stats = f
+
+
+def _mut_argmax_last(m):
+    def f(logits, drafts, kv_in, k):
+        x = np.asarray(logits, dtype=np.float64)
+        a = x.shape[1] - 1 - np.argmax(x[:, ::-1], axis=1)
+        R = len(kv_in)
+        n = np.zeros(R, np.int64)
+        for r in range(R):
+            while n[r] < k and drafts[r][n[r]] == a[r * (k + 1) + n[r]]:
+                n[r] += 1
+        return a, n, a[np.arange(R) * (k + 1) + n], np.asarray(kv_in) - (k - n)
+    m.ref_greedy_verify = f
+
+
+def _mut_draft_position(m):
+    def f(logits, drafts, kv_in, k):
+        a = np.argmax(np.asarray(logits, dtype=np.float64), axis=1)
+        R = len(kv_in)
+        n = np.zeros(R, np.int64)
+        for r in range(R):
+            while n[r] < k and drafts[r][n[r]] == a[r * (k + 1) + n[r] + 1]:
+                n[r] += 1
+        return a, n, a[np.arange(R) * (k + 1) + n], np.asarray(kv_in) - (k - n)
+    m.ref_greedy_verify = f
+
+
+def _mut_trim(m):
+    orig = m.ref_greedy_verify
+
+    def f(logits, drafts, kv_in, k):
+        a, n, nxt, kv = orig(logits, drafts, kv_in, k)
+        return a, n, nxt, np.asarray(kv_in) - n
+    m.ref_greedy_verify = f
+
+
+def _mut_unnormalised_merge(m):
+    def f(part_o, part_lse, gate=None):
+        part_o = np.asarray(part_o, dtype=np.float64)
+        part_lse = np.asarray(part_lse, dtype=np.float64)
+        m_ = part_lse.max(axis=0)
+        empty = ~np.isfinite(m_)
+        ms = np.where(empty, 0.0, m_)
+        w = np.where(empty[None], 0.0, np.exp(part_lse - ms[None]))
+        z = w.sum(axis=0)
+        lse = np.where(empty, -np.inf, ms + np.log(np.where(empty, 1.0, z)))
+        o = (w[..., None] * part_o).sum(axis=0)
+        if gate is not None:
+            o = m.sigmoid(m._as_f64(gate)) * o
+        return o, lse
+    m.ref_lse_combine = f
+
+
+def _mut_nan_identity(m):
+    orig = m._softmax_stats
+
+    def f(s, rows):
+        if s.shape[1] == 0:
+            return np.full(s.shape[0], -np.inf), np.full((s.shape[0], rows.shape[1]), np.nan)
+        return orig(s, rows)
+    m._softmax_stats = f
+
+
+MUTATIONS = [
+    _mut_bound_off_by_one, _mut_no_scale, _mut_gate_sign, _mut_token_mapping, _mut_lse_log2,
+    _mut_argmax_last, _mut_draft_position, _mut_trim, _mut_unnormalised_merge, _mut_nan_identity,
+]
+
+
+@pytest.mark.parametrize("mutate", MUTATIONS, ids=lambda f: f.__name__)
+def test_some_pin_catches(mutate):
+    m = _fresh_oracle()
+    mutate(m)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(m)
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught {mutate.__name__}"
