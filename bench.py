@@ -1,0 +1,381 @@
+"""Verify-step benchmark: one JSON line on stdout (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c1] [--impl reference]
+
+A step is one pass of the whole hot path on one synthetic batch: gated NoPE
+MLA verify attention (with its split-KV LSE merge) followed by the greedy
+verify (argmax, accepted prefix, trimmed kv_lens).  The default workload is
+the C=1 verify batch (1 request, k=7, 64 heads, context 1536, 163840-token
+vocabulary).  Inputs sit in HBM before timing; L2 (129 MB) is flushed by
+writing a 512 MB buffer before every timed step, outside the timed events.
+
+--impl reference times the float64 CPU oracle on the same workload (host
+cores).  Under torchrun (N > 1) every rank runs an independent replica (the
+verify step has no exchange between requests); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify-step µs & attention TFLOP/s (frac of peak); greedy-verify GB/s, 1×GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="c1")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_figures(inp):
+    """Algorithmic work of one step (counted on visible rows only)."""
+    H = inp["H"]
+    sum_b = int(inp["kv_bounds"].astype("int64").sum())
+    attn_flops = 4.0 * 512 * H * sum_b
+    k1 = inp["k"] + 1
+    kv_rows = 0
+    for r in range(inp["R"]):
+        kv_rows += int(inp["kv_bounds"][r * k1:(r + 1) * k1].max())
+    T = inp["T"]
+    attn_bytes = 1024.0 * kv_rows + T * H * (3 * 1024 + 4)
+    logits_bytes = 4.0 * T * inp["cfg"].vocab
+    return attn_flops, attn_bytes, logits_bytes
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verify_mla_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config_name):
+    """DRAM bytes per attention launch from a committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(config_name)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(config_name: str, min_seconds: float = 10.0, max_steps: int = 20):
+    """Time the float64 oracle on the host cores in a fresh process."""
+    cores = len(os.sched_getaffinity(0))
+    code = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+from workloads import make_inputs
+from oracle import ref_verify_step
+inp = make_inputs({config_name!r}, seed=0)
+ts = []
+t_end = time.perf_counter() + {min_seconds}
+while len(ts) < {max_steps} and (len(ts) < 2 or time.perf_counter() < t_end):
+    t0 = time.perf_counter(); ref_verify_step(inp); ts.append(time.perf_counter() - t0)
+print(json.dumps({{"per_step_s": sorted(ts)[len(ts)//2], "n": len(ts)}}))
+"""
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(cores)
+    res = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         timeout=600)
+    if res.returncode != 0:
+        return {"error": res.stderr.strip().splitlines()[-1:] or ["failed"]}
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    return {"value": d["per_step_s"] * 1e6, "unit": "us", "cores": cores, "kind": "oracle",
+            "sample": f"the whole {config_name} verify step (attention for all tokens and heads + "
+                      f"greedy verify), median of {d['n']} runs"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from workloads import CONFIGS
+    cfg = CONFIGS[args.config]
+    base = cpu_baseline(args.config, min_seconds=max(5.0, 0.5 * args.steps), max_steps=args.steps)
+    if "error" in base:
+        print(json.dumps({"impl": "reference", "unavailable": f"oracle run failed: {base['error']}"}))
+        return
+    v = base["value"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "us", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1000.0,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{cfg.name}: {cfg.description}"},
+        "cpu_baseline": base,
+        "e2e": {"value": v, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import numpy as np
+    import torch
+
+    import speculative_decoding_verify_mla_gb300 as sv
+    from workloads import CONFIGS, make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    sv.load_library()
+
+    cfg = CONFIGS[args.config]
+    inp = make_inputs(cfg, seed=rank)
+    R, k, H, T, V = inp["R"], inp["k"], inp["H"], inp["T"], cfg.vocab
+    attn_flops, attn_bytes, logits_bytes = workload_figures(inp)
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+    def i32(x):
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).to(device)
+
+    q, kv, gate = bf16(inp["q_bits"]), bf16(inp["kv_bits"]), bf16(inp["gate_bits"])
+    bt, bounds = i32(inp["block_table"]), i32(inp["kv_bounds"])
+    logits = torch.from_numpy(inp["logits"]).to(device)
+    drafts, kv_in = i32(inp["draft_tokens"]), i32(inp["kv_lens_in"])
+    step = sv.VerifyStep(device, R, k, H, V, inp["max_pages"], num_splits=args.splits)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+
+    def run_step():
+        return step(q, kv, bt, bounds, gate, inp["softmax_scale"], logits, drafts, kv_in)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def timed(fn, n):
+        """Per-call device time (ms) of fn, L2 flushed before each call."""
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            starts[i].record()
+            fn()
+            ends[i].record()
+        torch.cuda.synchronize()
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    for _ in range(max(3, args.warmup)):
+        run_step()
+    barrier()
+
+    sampler = ClockSampler(local)
+    if not args.no_clocks:
+        sampler.start()
+    barrier()
+    step_ms = timed(run_step, args.steps)
+    barrier()
+    attn_ms = timed(lambda: sv.mla_verify_decode(q, kv, bt, bounds, gate, k + 1, inp["softmax_scale"],
+                                                 num_splits=step.num_splits, workspace=step.attn_ws,
+                                                 out=step.out, lse=step.lse, status=step.status),
+                    args.steps)
+    greedy_ms = timed(lambda: sv.spec_verify_greedy(logits, drafts, kv_in, k, workspace=step.greedy_ws,
+                                                    argmax_ids=step.argmax, accepted=step.accepted,
+                                                    next_tokens=step.next_tokens,
+                                                    kv_lens_out=step.kv_lens_out), args.steps)
+    barrier()
+    clocks = sampler.stop() if not args.no_clocks else None
+
+    # end to end through the public API: pinned host inputs -> device, step, results -> host
+    host_in = {
+        "q": q.cpu().pin_memory(), "gate": gate.cpu().pin_memory(), "logits": logits.cpu().pin_memory(),
+        "bt": bt.cpu().pin_memory(), "bounds": bounds.cpu().pin_memory(),
+        "drafts": drafts.cpu().pin_memory(), "kv_in": kv_in.cpu().pin_memory(),
+    }
+    dev_in = {kk: torch.empty_like(v, device=device) for kk, v in host_in.items()}
+    host_out = [torch.empty(n, dtype=torch.int32).pin_memory() for n in (R, R, R)]
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out)
+
+    def e2e_step():
+        for kk, v in host_in.items():
+            dev_in[kk].copy_(v, non_blocking=True)
+        res = step(dev_in["q"], kv, dev_in["bt"], dev_in["bounds"], dev_in["gate"], inp["softmax_scale"],
+                   dev_in["logits"], dev_in["drafts"], dev_in["kv_in"])
+        for h, dvc in zip(host_out, (res[3], res[4], res[5])):
+            h.copy_(dvc, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e2e_ms = timed(e2e_step, args.steps)
+    barrier()
+
+    # max over ranks
+    def agg(xs):
+        m = statistics.mean(xs)
+        if world > 1:
+            t = torch.tensor([m], dtype=torch.float64, device=device)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            m = float(t.item())
+        return m
+
+    step_mean, attn_mean, greedy_mean, e2e_mean = (agg(step_ms), agg(attn_ms), agg(greedy_ms), agg(e2e_ms))
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peaks, peak_kind = load_peaks()
+    attn_tflops = attn_flops / (attn_mean * 1e-3) / 1e12
+    greedy_gbps = logits_bytes / (greedy_mean * 1e-3) / 1e9
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tensor_bound = attn_flops / attn_bytes > ridge
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        ach = attn_bytes / (attn_mean * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic(args.config)
+    roof["kernel"] = "mla_verify_decode call (attention kernel" + (" + LSE combine)" if step.num_splits > 1 else ")")
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json burst)" if peak_kind == "measured" else "fallback"
+    roof["algorithmic_per_launch"] = {"flops": attn_flops, "bytes": attn_bytes}
+
+    base = None
+    if not args.no_cpu_baseline:
+        base = cpu_baseline(args.config)
+
+    line = {
+        "metric": METRIC,
+        "value": step_mean * 1000.0,
+        "unit": "us",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_mean,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: {cfg.description}", "R": R, "k": k, "H": H, "T": T,
+                   "vocab": V, "latent": 512, "page": 64, "num_splits": step.num_splits,
+                   "l2": "flushed (512 MB write) before every timed step, outside the events",
+                   "parallelism": f"replicas x{world}"},
+        "attention_us": attn_mean * 1000.0,
+        "attention_tflops": attn_tflops,
+        "greedy_us": greedy_mean * 1000.0,
+        "greedy_gbps": greedy_gbps,
+        "greedy_hbm_frac": greedy_gbps / peaks["hbm_gbs"],
+        "steps_per_s_all_gpus": world * 1000.0 / step_mean,
+        "roofline": roof,
+        "cpu_baseline": base,
+        "e2e": {"value": e2e_mean * 1000.0, "unit": "us", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * step.launches_per_step,
+        "clocks": clocks,
+        "status_word": int(step.status.item()),
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

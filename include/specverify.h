@@ -1,0 +1,188 @@
+/*
+ * specverify.h - C ABI of the GB300 (sm_103a) speculative-decoding verify step
+ * for absorbed, gated NoPE MLA over a paged bf16 latent KV cache.
+ *
+ * One verify step: each of R requests feeds a verify group of 1 target token
+ * plus k drafted tokens ("M* PR #257: Kimi K3 support with DSpark speculative
+ * decoding", section "Speculative decoding").  T = R*(k+1) query tokens,
+ * H heads, latent width D = 512.
+ *
+ *   mla_verify_decode   attention of every token over its request's paged
+ *                       latent rows, bounded per token, split over KV, with
+ *                       the LSE merge and the sigmoid gate fused in.
+ *   mla_lse_combine     the LSE merge + gate of split partials on its own.
+ *   spec_verify_greedy  target argmax, accepted draft prefix, next token and
+ *                       trimmed per-request KV length.
+ *
+ * Conventions shared by every call:
+ *  - Every pointer named "device" is CUDA device memory owned by the caller;
+ *    the library never allocates, never frees and never synchronises the host.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream).
+ *  - Host-side argument checks run before any launch; a failed check returns
+ *    its sv_status code and launches nothing.
+ *  - Bad *device data* (a block-table entry outside the pool, a bound outside
+ *    [0, max_pages_per_req*page_size]) never traps: the kernel ORs an
+ *    SV_DEV_* bit into the caller's device status word, substitutes a safe
+ *    value (page 0, the clamped bound) and carries on; the outputs of that
+ *    call are then undefined.  The caller reads the status word.
+ *  - Every wait inside a kernel is bounded (about two seconds); a wait that
+ *    gives up ORs SV_DEV_TIMEOUT into the status word and the kernel returns.
+ */
+#ifndef SPECVERIFY_H_
+#define SPECVERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* sv_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_NULL = 1,        /* a required pointer is NULL                       */
+  SV_ERR_SHAPE = 2,       /* a size is negative or inconsistent               */
+  SV_ERR_ALIGN = 3,       /* a pointer misses its required alignment          */
+  SV_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required       */
+  SV_ERR_UNSUPPORTED = 5, /* valid but unsupported (page_size != 64, D != 512) */
+  SV_ERR_LAUNCH = 6,      /* the CUDA launch itself failed                    */
+  SV_ERR_DEVICE_DATA = 7, /* reserved for callers mapping SV_DEV_* bits       */
+  SV_ERR_TIMEOUT = 8,     /* reserved for callers mapping SV_DEV_TIMEOUT      */
+  SV_ERR_DEVICE = 9       /* no usable sm_103a device / attribute query failed */
+} sv_status;
+
+/* bits ORed into the device status word */
+#define SV_DEV_BAD_PAGE  0x1  /* block_table entry < 0 or >= num_pages was needed */
+#define SV_DEV_BAD_BOUND 0x2  /* kv_bounds[t] < 0 or > max_pages_per_req*page_size */
+#define SV_DEV_TIMEOUT   0x4  /* a bounded in-kernel wait gave up                 */
+
+#define SV_LATENT_DIM 512
+#define SV_PAGE_SIZE 64
+#define SV_MAX_SPLITS 64
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* sv_status_string(sv_status s);
+
+/* ------------------------------------------------------------------------
+ * mla_verify_decode
+ *
+ * Absorbed, gated NoPE MLA decode attention for verify groups ("M* PR #257",
+ * section "Model": gated NoPE MLA with absorbed projections), with the
+ * per-token attention bound, the widened masked span and the (-inf, 0)
+ * stats identity of "TensorRT-LLM PR #18166: Kimi K3 DSpark speculative
+ * decoding under Helix CP" (first commit message and Summary).
+ *
+ * For token t (request r = t / q_per_req) and head h, with b = kv_bounds[t]
+ * and c_j the latent row of KV position j (page block_table[r][j/64], slot
+ * j%64):
+ *     s_j  = softmax_scale * <q[t][h], c_j>              for j < b
+ *     lse  = ln sum_j exp(s_j)                           (-inf when b == 0)
+ *     o    = sum_j exp(s_j - lse) * c_j                  (0    when b == 0)
+ *     out  = sigmoid(gate[t][h]) * o   (elementwise over the 512 columns)
+ * The k+1 tokens of a request are folded into M = H*(k+1) query rows that
+ * share the request's KV (row = t_local*H + h), processed as 128-row tiles.
+ *
+ * Arguments (all device pointers unless stated):
+ *   q_latent      bf16 [T][H][512], 16-byte aligned, contiguous.
+ *   kv_pages      bf16 [num_pages][page_size][512], 16-byte aligned
+ *                 (the page pool; read through a TMA tensor map).
+ *   num_pages     pool size in pages (>= 1 when any bound is > 0).
+ *   page_size     must be 64 (else SV_ERR_UNSUPPORTED).
+ *   block_table   int32 [R][max_pages_per_req]: page ids; entries past a
+ *                 request's last needed page are never read.
+ *   R, q_per_req  requests and tokens per request (k+1 >= 1); T = R*q_per_req.
+ *   kv_bounds     int32 [T]: token t sees positions j < kv_bounds[t];
+ *                 0 <= kv_bounds[t] <= max_pages_per_req*page_size.
+ *   gate          bf16 [T][H][512].
+ *   H             heads, >= 1.
+ *   softmax_scale scale of the scores (finite, > 0).
+ *   num_splits    KV splits per (request, row tile): 0 = automatic, else
+ *                 1..SV_MAX_SPLITS.  Split s of request r covers KV tiles
+ *                 [s*n_r/S, (s+1)*n_r/S) (integer division) with
+ *                 n_r = ceil(max_t kv_bounds[t] / 64) over r's tokens.
+ *   workspace     device scratch of at least
+ *                 sv_mla_verify_workspace_bytes(T, H, S) bytes (S = the split
+ *                 count used; sv_mla_verify_num_splits gives the automatic
+ *                 one), 256-byte aligned; may be NULL when S == 1.  Holds the
+ *                 split partials, layout part_o fp32 [S][T][H][512] followed
+ *                 by part_lse fp32 [S][T][H] (lse of the split's KV range,
+ *                 natural log, -inf for an empty range; part_o normalised
+ *                 within the split, 0 for an empty range).
+ *   workspace_bytes  its size in bytes.
+ *   out           bf16 [T][H][512] (round to nearest even).
+ *   lse           fp32 [T][H], natural log of the ungated scaled scores.
+ *   status        device int32, ORed with SV_DEV_* bits; may be NULL.
+ *   stream        CUDA stream.
+ * Returns SV_OK after enqueueing, or the first failed check.
+ * ---------------------------------------------------------------------- */
+/* The split count num_splits = 0 resolves to on the current device (it only
+ * looks at the sizes, never at device data). */
+int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pages_per_req);
+size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits);
+
+sv_status mla_verify_decode(const void* q_latent, const void* kv_pages, int num_pages,
+                            int page_size, const int32_t* block_table, int R, int q_per_req,
+                            int max_pages_per_req, const int32_t* kv_bounds, const void* gate,
+                            int H, float softmax_scale, int num_splits, void* workspace,
+                            size_t workspace_bytes, void* out, float* lse, int32_t* status,
+                            sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * mla_lse_combine
+ *
+ * Merge of split-KV partials by their log-sum-exp (the CP / DCP LSE merge of
+ * "TensorRT-LLM PR #18166", second and third commit messages, and of the vLLM
+ * page "kimi_k3/nvidia/specialized_decode/drafter/model", DraftDcp), plus the
+ * sigmoid-gate epilogue:
+ *     lse = ln sum_s exp(part_lse[s])
+ *     o   = sum_s exp(part_lse[s] - lse) * part_o[s]
+ *     out = sigmoid(gate) * o
+ * A row whose partials are all -inf gives lse = -inf and out = 0 (never NaN).
+ *
+ *   part_o    fp32 [S][T][H][512], 16-byte aligned.
+ *   part_lse  fp32 [S][T][H].
+ *   S         1..SV_MAX_SPLITS;  T, H >= 0.
+ *   gate      bf16 [T][H][512], 8-byte aligned.
+ *   out       bf16 [T][H][512], 8-byte aligned;  lse fp32 [T][H].
+ * ---------------------------------------------------------------------- */
+sv_status mla_lse_combine(const float* part_o, const float* part_lse, int S, int T, int H,
+                          const void* gate, void* out, float* lse, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * spec_verify_greedy
+ *
+ * Greedy verification with KV trim ("M* PR #257", section "Speculative
+ * decoding": verification is greedy, the KV trims rejected tails):
+ *     a[t]          = argmax_v logits[t][v]     (lowest v on ties; -0 == +0)
+ *     accepted[r]   = n = largest m <= k with draft_tokens[r][j-1] == a[r*(k+1)+j-1]
+ *                     for every j = 1..m
+ *     next_tokens[r]= a[r*(k+1) + n]
+ *     kv_lens_out[r]= kv_lens_in[r] - (k - n)
+ * kv_lens_in counts the k+1 verify tokens already written to the cache.
+ *
+ *   logits        fp32 [T][V], T = R*(k+1), V >= 1; values must be finite.
+ *   draft_tokens  int32 [R][k] (may be NULL when k == 0).
+ *   kv_lens_in    int32 [R].
+ *   argmax_ids    int32 [T]; accepted, next_tokens, kv_lens_out int32 [R].
+ *   workspace     device scratch of sv_greedy_workspace_bytes(T, V) bytes,
+ *                 256-byte aligned.  It must be zero-filled before its first
+ *                 use (e.g. cudaMemsetAsync); every call leaves it zero-filled
+ *                 again, so one zeroing serves any number of later calls on
+ *                 the same stream.  Calls sharing one workspace must not run
+ *                 concurrently.
+ * ---------------------------------------------------------------------- */
+size_t sv_greedy_workspace_bytes(int T, int V);
+
+sv_status spec_verify_greedy(const float* logits, int T, int V, int R, int k,
+                             const int32_t* draft_tokens, const int32_t* kv_lens_in,
+                             int32_t* argmax_ids, int32_t* accepted, int32_t* next_tokens,
+                             int32_t* kv_lens_out, void* workspace, size_t workspace_bytes,
+                             sv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H_ */

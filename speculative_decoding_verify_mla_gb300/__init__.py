@@ -1,0 +1,22 @@
+"""GB300-native speculative-decoding verify step for gated NoPE MLA.
+
+The compute lives in ``libspecverify.so`` (hand-written sm_103a CUDA, C ABI in
+``include/specverify.h``); this package is the thin Python binding.
+"""
+from .binding import (  # noqa: F401
+    EXPORTED_SYMBOLS,
+    SV_DEV_BAD_BOUND,
+    SV_DEV_BAD_PAGE,
+    SV_DEV_TIMEOUT,
+    SpecVerifyError,
+    attention_workspace_bytes,
+    greedy_workspace,
+    greedy_workspace_bytes,
+    load_library,
+    mla_lse_combine,
+    mla_verify_decode,
+    num_splits_for,
+    spec_verify_greedy,
+    status_string,
+)
+from .step import VerifyStep  # noqa: F401

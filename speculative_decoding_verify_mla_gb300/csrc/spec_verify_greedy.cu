@@ -1,0 +1,190 @@
+// spec_verify_greedy.cu - greedy verification of drafted tokens with KV trim.
+//
+// Definition ("M* PR #257: Kimi K3 support with DSpark speculative decoding",
+// section "Speculative decoding": verification is greedy, the KV trims the
+// rejected tails): a[t] = argmax_v logits[t][v] with the lowest v on ties;
+// request r accepts the longest prefix of its k drafts with d_j == a_{j-1};
+// next token a_n; kv_lens_out = kv_lens_in - (k - n).
+//
+// One launch.  The [T][V] fp32 logits are cut into chunks of C floats; each
+// CTA streams one chunk with coalesced 128-bit loads, reduces it to a 64-bit
+// key (order-preserving value bits << 32 | ~index, so the max key is the max
+// value at the lowest index) with warp shuffles, and parks the key in the
+// workspace.  The CTA that takes the last ticket reduces the keys per row,
+// writes the argmax ids, scans the drafts of every request and resets the
+// ticket to zero.  Nothing waits on another CTA.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "specverify.h"
+
+namespace sv {
+namespace {
+
+constexpr int kGreedyThreads = 256;
+constexpr size_t kGreedyHeader = 256;  // ticket counter, padded
+
+__device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;  // -0 and +0 compare equal
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, k, o);
+    k = other > k ? other : k;
+  }
+  return k;
+}
+
+__global__ void __launch_bounds__(kGreedyThreads)
+    greedy_verify_kernel(const float* __restrict__ logits, int T, int V, int R, int k,
+                         int chunk, int nchunks, bool vec4,
+                         const int32_t* __restrict__ draft_tokens,
+                         const int32_t* __restrict__ kv_lens_in, int32_t* __restrict__ argmax_ids,
+                         int32_t* __restrict__ accepted, int32_t* __restrict__ next_tokens,
+                         int32_t* __restrict__ kv_lens_out, unsigned int* __restrict__ ticket,
+                         unsigned long long* __restrict__ keys) {
+  __shared__ unsigned long long s_warp[kGreedyThreads / 32];
+  __shared__ bool s_last;
+  const int tid = threadIdx.x;
+  const long long bid = blockIdx.x;
+  const int t = (int)(bid / nchunks);
+  const int c = (int)(bid % nchunks);
+  const long long lo = (long long)c * chunk;
+  const long long hi = min((long long)V, lo + chunk);
+  const float* row = logits + (long long)t * V;
+
+  // ---- chunk scan: each thread walks its elements in increasing index order
+  float best_v = -INFINITY;
+  uint32_t best_i = 0xFFFFFFFFu;
+  if (vec4) {
+    const float4* p4 = reinterpret_cast<const float4*>(row + lo);
+    const int n4 = (int)((hi - lo) >> 2);
+    int i = tid;
+    for (; i + 3 * kGreedyThreads < n4; i += 4 * kGreedyThreads) {
+      float4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = __ldcs(p4 + i + u * kGreedyThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t base = (uint32_t)(lo + 4ll * (i + u * kGreedyThreads));
+        if (best_i == 0xFFFFFFFFu) { best_v = a[u].x; best_i = base; }
+        else if (a[u].x > best_v) { best_v = a[u].x; best_i = base; }
+        if (a[u].y > best_v) { best_v = a[u].y; best_i = base + 1; }
+        if (a[u].z > best_v) { best_v = a[u].z; best_i = base + 2; }
+        if (a[u].w > best_v) { best_v = a[u].w; best_i = base + 3; }
+      }
+    }
+    for (; i < n4; i += kGreedyThreads) {
+      const float4 a = __ldcs(p4 + i);
+      const uint32_t base = (uint32_t)(lo + 4ll * i);
+      if (best_i == 0xFFFFFFFFu) { best_v = a.x; best_i = base; }
+      else if (a.x > best_v) { best_v = a.x; best_i = base; }
+      if (a.y > best_v) { best_v = a.y; best_i = base + 1; }
+      if (a.z > best_v) { best_v = a.z; best_i = base + 2; }
+      if (a.w > best_v) { best_v = a.w; best_i = base + 3; }
+    }
+  } else {
+    for (long long i = lo + tid; i < hi; i += kGreedyThreads) {
+      const float x = __ldcs(row + i);
+      if (best_i == 0xFFFFFFFFu || x > best_v) { best_v = x; best_i = (uint32_t)i; }
+    }
+  }
+  unsigned long long key = (best_i == 0xFFFFFFFFu) ? 0ull : argmax_key(best_v, best_i);
+  key = warp_max_u64(key);
+  if ((tid & 31) == 0) s_warp[tid >> 5] = key;
+  __syncthreads();
+  if (tid < 32) {
+    unsigned long long kk = tid < kGreedyThreads / 32 ? s_warp[tid] : 0ull;
+    kk = warp_max_u64(kk);
+    if (tid == 0) {
+      keys[(long long)t * nchunks + c] = kk;
+      __threadfence();
+      const unsigned int prev = atomicAdd(ticket, 1u);
+      s_last = (prev == gridDim.x - 1);
+    }
+  }
+  __syncthreads();
+  if (!s_last) return;
+
+  // ---- last CTA: per-row argmax, then acceptance and trim per request
+  __threadfence();
+  for (int tt = tid; tt < T; tt += kGreedyThreads) {
+    unsigned long long best = 0ull;
+    const unsigned long long* kr = keys + (long long)tt * nchunks;
+    for (int j = 0; j < nchunks; ++j) {
+      const unsigned long long x = __ldcg(kr + j);
+      best = x > best ? x : best;
+    }
+    argmax_ids[tt] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+  }
+  __syncthreads();
+  for (int r = tid; r < R; r += kGreedyThreads) {
+    const int base = r * (k + 1);
+    int n = 0;
+    while (n < k && __ldcg(draft_tokens + (long long)r * k + n) == argmax_ids[base + n]) ++n;
+    accepted[r] = n;
+    next_tokens[r] = argmax_ids[base + n];
+    kv_lens_out[r] = kv_lens_in[r] - (k - n);
+  }
+  if (tid == 0) *ticket = 0u;  // leave the workspace zeroed for the next call
+}
+
+// Chunk length (floats) as a function of the problem only, so that the
+// workspace query and the launch agree.
+int greedy_chunk(int T, int V) {
+  const long long total = (long long)T * V;
+  long long c = (total + 8 * 152 - 1) / (8 * 152);
+  c = (c + 2047) / 2048 * 2048;
+  if (c < 2048) c = 2048;
+  if (c > 32768) c = 32768;
+  return (int)c;
+}
+
+}  // namespace
+}  // namespace sv
+
+extern "C" size_t sv_greedy_workspace_bytes(int T, int V) {
+  if (T <= 0 || V <= 0) return sv::kGreedyHeader;
+  const int chunk = sv::greedy_chunk(T, V);
+  const long long nchunks = (V + (long long)chunk - 1) / chunk;
+  return sv::kGreedyHeader + (size_t)T * (size_t)nchunks * sizeof(unsigned long long);
+}
+
+extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R, int k,
+                                        const int32_t* draft_tokens, const int32_t* kv_lens_in,
+                                        int32_t* argmax_ids, int32_t* accepted,
+                                        int32_t* next_tokens, int32_t* kv_lens_out,
+                                        void* workspace, size_t workspace_bytes,
+                                        sv_stream_t stream) {
+  if (T < 0 || R < 0 || k < 0) return SV_ERR_SHAPE;
+  if ((long long)R * (k + 1) != (long long)T) return SV_ERR_SHAPE;
+  if (T == 0) return SV_OK;
+  if (V < 1) return SV_ERR_SHAPE;
+  if ((long long)V > 0x7FFFFFFFll - 32768) return SV_ERR_SHAPE;
+  if (!logits || !kv_lens_in || !argmax_ids || !accepted || !next_tokens || !kv_lens_out ||
+      !workspace)
+    return SV_ERR_NULL;
+  if (k > 0 && !draft_tokens) return SV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return SV_ERR_ALIGN;
+  if (workspace_bytes < sv_greedy_workspace_bytes(T, V)) return SV_ERR_WORKSPACE;
+  const int chunk = sv::greedy_chunk(T, V);
+  const int nchunks = (int)((V + (long long)chunk - 1) / chunk);
+  const long long blocks = (long long)T * nchunks;
+  if (blocks > 0x7FFFFFFFll) return SV_ERR_SHAPE;
+  const bool vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
+  auto* ticket = reinterpret_cast<unsigned int*>(workspace);
+  auto* keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
+                                                     sv::kGreedyHeader);
+  sv::greedy_verify_kernel<<<(unsigned)blocks, sv::kGreedyThreads, 0,
+                             reinterpret_cast<cudaStream_t>(stream)>>>(
+      logits, T, V, R, k, chunk, nchunks, vec4, draft_tokens, kv_lens_in, argmax_ids, accepted,
+      next_tokens, kv_lens_out, ticket, keys);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_LAUNCH;
+}

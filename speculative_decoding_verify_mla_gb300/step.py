@@ -1,0 +1,49 @@
+"""One whole verify step (attention + greedy verify) on preallocated buffers."""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class VerifyStep:
+    """Runs mla_verify_decode then spec_verify_greedy on one stream.
+
+    Output buffers and both workspaces are allocated once (torch) and reused,
+    so a step enqueues exactly the library's kernels and nothing else."""
+
+    def __init__(self, device, R: int, k: int, H: int, V: int, max_pages: int,
+                 num_splits: int = 0):
+        device = torch.device(device)
+        self.device = device
+        self.R, self.k, self.H, self.V = R, k, H, V
+        self.T = R * (k + 1)
+        self.max_pages = max_pages
+        self.num_splits = num_splits or B.num_splits_for(R, k + 1, H, max_pages)
+        T = self.T
+        self.out = torch.empty((T, H, B.SV_LATENT_DIM), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((T, H), dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        ws = B.attention_workspace_bytes(T, H, self.num_splits)
+        self.attn_ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        self.greedy_ws = torch.zeros(B.greedy_workspace_bytes(T, V), dtype=torch.uint8,
+                                     device=device)
+        self.argmax = torch.empty(T, dtype=torch.int32, device=device)
+        self.accepted = torch.empty(R, dtype=torch.int32, device=device)
+        self.next_tokens = torch.empty(R, dtype=torch.int32, device=device)
+        self.kv_lens_out = torch.empty(R, dtype=torch.int32, device=device)
+
+    def __call__(self, q_latent, kv_pages, block_table, kv_bounds, gate, softmax_scale,
+                 logits, draft_tokens, kv_lens_in):
+        B.mla_verify_decode(q_latent, kv_pages, block_table, kv_bounds, gate, self.k + 1,
+                            softmax_scale, num_splits=self.num_splits, workspace=self.attn_ws,
+                            out=self.out, lse=self.lse, status=self.status)
+        B.spec_verify_greedy(logits, draft_tokens, kv_lens_in, self.k, workspace=self.greedy_ws,
+                             argmax_ids=self.argmax, accepted=self.accepted,
+                             next_tokens=self.next_tokens, kv_lens_out=self.kv_lens_out)
+        return self.out, self.lse, self.argmax, self.accepted, self.next_tokens, self.kv_lens_out
+
+    @property
+    def launches_per_step(self) -> int:
+        """Kernels one step enqueues: attention (+ combine when split) + greedy."""
+        return 1 + (1 if self.num_splits > 1 else 0) + 1

@@ -1,0 +1,104 @@
+"""The C ABI library: it builds, loads and exports every declared symbol, and
+its host-side argument checks reject bad calls before any launch (CPU only:
+no call here reaches the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verify_mla_gb300 import build as B
+    B.build()
+    from speculative_decoding_verify_mla_gb300 import load_library
+    return load_library()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for f in ("mla_verify_decode", "mla_lse_combine", "spec_verify_greedy"):
+        assert f in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from speculative_decoding_verify_mla_gb300 import EXPORTED_SYMBOLS
+    names = declared_functions()
+    assert set(EXPORTED_SYMBOLS) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    from speculative_decoding_verify_mla_gb300 import status_string
+    assert status_string(0) == "ok"
+    assert "workspace" in status_string(4)
+    assert status_string(99) == "unknown status"
+
+
+def test_workspace_queries(lib):
+    from speculative_decoding_verify_mla_gb300 import attention_workspace_bytes, greedy_workspace_bytes
+    assert attention_workspace_bytes(8, 64, 1) == 0
+    assert attention_workspace_bytes(8, 64, 3) == 3 * 8 * 64 * (512 + 1) * 4
+    assert greedy_workspace_bytes(8, 163840) >= 256 + 8 * 8
+    assert greedy_workspace_bytes(0, 10) == 256
+
+
+def _attn_call(lib, **kw):
+    args = dict(q=1 << 12, kv=1 << 12, num_pages=4, page_size=64, bt=1 << 12, R=2, qpr=4, maxp=2,
+                bounds=1 << 12, gate=1 << 12, H=8, scale=0.1, splits=1, ws=None, ws_bytes=0,
+                out=1 << 12, lse=1 << 12, status=None, stream=None)
+    args.update(kw)
+    return lib.mla_verify_decode(args["q"], args["kv"], args["num_pages"], args["page_size"], args["bt"],
+                                 args["R"], args["qpr"], args["maxp"], args["bounds"], args["gate"],
+                                 args["H"], ctypes.c_float(args["scale"]), args["splits"], args["ws"],
+                                 args["ws_bytes"], args["out"], args["lse"], args["status"], args["stream"])
+
+
+def test_attention_host_checks(lib):
+    # every failure below is decided before any CUDA call
+    assert _attn_call(lib, page_size=32) == 5          # unsupported page size
+    assert _attn_call(lib, R=-1) == 2
+    assert _attn_call(lib, qpr=0) == 2
+    assert _attn_call(lib, H=0) == 2
+    assert _attn_call(lib, splits=65) == 2
+    assert _attn_call(lib, R=0) == 0                  # empty batch: nothing to do
+    assert _attn_call(lib, scale=float("nan")) == 2
+    assert _attn_call(lib, scale=-1.0) == 2
+    assert _attn_call(lib, num_pages=0) == 2
+    assert _attn_call(lib, q=None) == 1
+    assert _attn_call(lib, lse=None) == 1
+    assert _attn_call(lib, q=(1 << 12) + 8) == 3       # q must be 16-byte aligned
+    assert _attn_call(lib, out=(1 << 12) + 2) == 3
+
+
+def test_combine_host_checks(lib):
+    assert lib.mla_lse_combine(None, None, 0, 1, 1, None, None, None, None) == 2
+    assert lib.mla_lse_combine(None, None, 2, 0, 8, None, None, None, None) == 0
+    assert lib.mla_lse_combine(None, 4096, 2, 1, 8, 4096, 4096, 4096, None) == 1
+    assert lib.mla_lse_combine(4096 + 4, 4096, 2, 1, 8, 4096, 4096, 4096, None) == 3
+
+
+def test_greedy_host_checks(lib):
+    f = lib.spec_verify_greedy
+    assert f(4096, 7, 10, 2, 3, 4096, 4096, 4096, 4096, 4096, 4096, 4096, 1 << 20, None) == 2  # T != R(k+1)
+    assert f(4096, 0, 10, 0, 3, None, None, None, None, None, None, None, 0, None) == 0
+    assert f(4096, 8, 0, 2, 3, 4096, 4096, 4096, 4096, 4096, 4096, 4096, 1 << 20, None) == 2  # V = 0
+    assert f(None, 8, 10, 2, 3, 4096, 4096, 4096, 4096, 4096, 4096, 4096, 1 << 20, None) == 1
+    assert f(4096, 8, 10, 2, 3, None, 4096, 4096, 4096, 4096, 4096, 4096, 1 << 20, None) == 1  # drafts
+    assert f(4096, 8, 10, 2, 3, 4096, 4096, 4096, 4096, 4096, 4096, 4096, 8, None) == 4      # workspace
+    assert f(4096, 8, 10, 2, 3, 4096, 4096, 4096, 4096, 4096, 4096, 4096 + 16, 1 << 20, None) == 3
