@@ -152,7 +152,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(config_name: str, min_seconds: float = 10.0, max_steps: int = 20):
+def cpu_baseline(config_name: str, min_seconds: float = 10.0, max_steps: int = 1000):
     """Time the float64 oracle on the host cores in a fresh process."""
     cores = len(os.sched_getaffinity(0))
     code = f"""
