@@ -181,6 +181,33 @@ sv_status spec_verify_greedy(const float* logits, int T, int V, int R, int k,
                              int32_t* kv_lens_out, void* workspace, size_t workspace_bytes,
                              sv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * spec_verify_greedy_noalloc
+ *
+ * The paper has no counterpart to this call: it is an addition for callers
+ * that cannot allocate device memory when they verify (for example a serving
+ * engine that has reserved nearly all HBM for its own KV-cache pool, or a
+ * plugin whose host framework owns the device allocator) and so cannot pass
+ * the workspace spec_verify_greedy needs.
+ *
+ * Same arguments, results and errors as spec_verify_greedy, without the
+ * workspace.  The scratch lives in a file-scope device array of 512 KiB that
+ * every GPU loading this library keeps until the process exits.
+ *  - A problem with sv_greedy_workspace_bytes(T, V) > 512 KiB is rejected with
+ *    SV_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on a device looks up the array's address with that device
+ *    current; make that first call before any stream capture begins.
+ *  - Each call clears the array's counter with cudaMemsetAsync on `stream`
+ *    before its kernel; nothing is allocated or freed.
+ *  - All calls share the one array: calls whose kernels may overlap on the
+ *    GPU (unordered streams, several host threads) race and give wrong
+ *    results.  Calls in order on one stream are safe.
+ * ---------------------------------------------------------------------- */
+sv_status spec_verify_greedy_noalloc(const float* logits, int T, int V, int R, int k,
+                                     const int32_t* draft_tokens, const int32_t* kv_lens_in,
+                                     int32_t* argmax_ids, int32_t* accepted, int32_t* next_tokens,
+                                     int32_t* kv_lens_out, sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "specverify.h"
 
@@ -187,4 +188,80 @@ extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R
       logits, T, V, R, k, chunk, nchunks, vec4, draft_tokens, kv_lens_in, argmax_ids, accepted,
       next_tokens, kv_lens_out, ticket, keys);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.
+//
+// Some callers cannot allocate device memory at the point where they verify:
+// a serving engine that has already handed (nearly) all of HBM to its own
+// KV-cache pool and forbids further cudaMalloc calls, or a plugin hosted by a
+// framework that owns the device allocator.  Such a caller cannot provide the
+// greedy workspace.  This entry point keeps that scratch (the ticket counter
+// and the per-chunk argmax keys) in a fixed file-scope device array instead.
+//
+// Limits and sharing:
+//  * The array holds kNoAllocScratchBytes (512 KiB) on every GPU that loads
+//    this library, until the process exits.  A problem whose workspace
+//    (sv_greedy_workspace_bytes(T, V)) is larger is rejected with
+//    SV_ERR_WORKSPACE before anything is enqueued.
+//  * Every call shares the one array: calls whose kernels could overlap on the
+//    GPU (different streams without ordering, or several host threads) race
+//    on it and give wrong results.  Calls issued in order on one stream are
+//    fine.
+//  * The first call on a device looks up the array's device address
+//    (cudaGetSymbolAddress) with that device current and caches it; make that
+//    first call before any stream capture begins.
+//  * The ticket counter must start at zero: each call clears it with a
+//    cudaMemsetAsync on the same stream before the kernel runs.  The keys need
+//    no initial value.
+// No cudaMalloc, cudaFree or other allocating routine is called.
+namespace sv {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 512 * 1024;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64];
+
+// Device address of g_noalloc_scratch on the current device (nullptr on failure).
+void* noalloc_scratch_for_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace sv
+
+extern "C" sv_status spec_verify_greedy_noalloc(const float* logits, int T, int V, int R, int k,
+                                                const int32_t* draft_tokens,
+                                                const int32_t* kv_lens_in, int32_t* argmax_ids,
+                                                int32_t* accepted, int32_t* next_tokens,
+                                                int32_t* kv_lens_out, sv_stream_t stream) {
+  if (T < 0 || R < 0 || k < 0) return SV_ERR_SHAPE;
+  if ((long long)R * (k + 1) != (long long)T) return SV_ERR_SHAPE;
+  if (T == 0) return SV_OK;
+  if (V < 1) return SV_ERR_SHAPE;
+  const size_t need = sv_greedy_workspace_bytes(T, V);
+  if (need > sv::kNoAllocScratchBytes) return SV_ERR_WORKSPACE;
+  void* scratch = sv::noalloc_scratch_for_current_device();
+  if (!scratch) return SV_ERR_DEVICE;
+  if (cudaMemsetAsync(scratch, 0, sv::kGreedyHeader, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_LAUNCH;
+  }
+  return spec_verify_greedy(logits, T, V, R, k, draft_tokens, kv_lens_in, argmax_ids, accepted,
+                            next_tokens, kv_lens_out, scratch, sv::kNoAllocScratchBytes, stream);
 }
