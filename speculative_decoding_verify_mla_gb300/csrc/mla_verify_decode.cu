@@ -1,5 +1,5 @@
 // mla_verify_decode.cu - absorbed, gated NoPE MLA verify-decode attention over
-// a paged bf16 latent KV cache, for sm_103a (tcgen05 + TMEM + TMA + clusters).
+// a paged bf16 latent KV cache, for sm_103a (tcgen05 + TMEM + TMA).
 //
 // What it computes ("M* PR #257: Kimi K3 support with DSpark speculative
 // decoding", sections "Model" and "Speculative decoding"; per-token bounds,
@@ -13,29 +13,30 @@
 // Design (one GPU, sm_103a):
 //  * Fold.  The k+1 tokens of a request times H heads are M = H (k+1) query
 //    rows sharing one KV stream (row = t*H + h).  A work unit is (request,
-//    128-row tile, KV split) and runs on a 2-CTA cluster.
-//  * Latent split across the pair.  An fp32 128 x 512 output tile would fill
-//    the whole 512-column TMEM of one SM, so CTA c of the pair owns latent
-//    columns [256c, 256c + 256): its TMEM holds O[:, half c] (256 columns),
-//    its half of Q as a bf16 A operand (128 columns) and two 64-column score
-//    buffers.  Because K = V (absorbed MLA), the same half of each KV row
-//    feeds both of its GEMMs, so each CTA streams exactly half of every
-//    latent row: the pair reads the KV once.
-//  * Scores.  CTA c computes the partial scores Q[:, half c] K[:, half c]^T
-//    (tcgen05.mma, M=128, N=64, K=256, A from TMEM, B from swizzled SMEM);
-//    the two partials are swapped through distributed shared memory and
-//    added (fp32, a+b in both CTAs, so both see bit-identical scores).
+//    128-row tile, KV split, latent half) and runs on one CTA.
+//  * Latent halves.  An fp32 128 x 512 output tile would fill the whole
+//    512-column TMEM of one SM, so a CTA owns latent columns [256c, 256c+256)
+//    of O (256 TMEM columns).  Its TMEM also holds its own half of Q as a bf16
+//    A operand (128 columns) and two 64-column score buffers.
+//  * Scores.  The CTA computes the full 128 x 64 score tile of each 64-row KV
+//    tile: Q[:, own] K[:, own]^T with A from TMEM (tcgen05.mma kind::f16,
+//    M=128, N=64) plus Q[:, other] K[:, other]^T with A from swizzled SMEM.
+//    Both halves of a unit therefore compute the same scores (1.5x the
+//    algorithmic tensor work), but no CTA ever waits on another SM.
 //  * Softmax.  One thread per query row: scale, per-token bound mask, running
 //    max with a lazy rescale (O is rescaled in TMEM only when the max grows by
 //    more than 2^8), exp2, bf16 P written back into the score buffer in TMEM.
 //  * P V.  tcgen05.mma M=128, N=256, K=64 with A = P from TMEM and B = the
-//    same SMEM tile read MN-major (V = the latent rows).
+//    own-half KV tile read MN-major (V = the latent rows, absorbed MLA).
 //  * KV.  TMA tiled loads of 64 rows x 64 columns (128-byte swizzle) from a
 //    2-D tensor map over the page pool; the row coordinate is page * 64, so
-//    the block table is applied per tile.  4-stage ring.  Pool slack beyond
-//    the tile's largest bound is zeroed in SMEM before use (0 * NaN safety).
-//  * Epilogue.  One split: normalise, gate, bf16 out + lse.  Several splits:
-//    fp32 partials (o/l, lse) for mla_lse_combine.
+//    the block table is applied per tile.  The own half (used by the scores
+//    and by P V) sits in a 3-stage ring; the other half (scores only) in a
+//    2-stage ring that is released as soon as the score MMA completes.  Pool
+//    slack beyond the tile's largest bound is zeroed in SMEM before use
+//    (0 * NaN safety).
+//  * Epilogue.  One split: normalise, gate (prefetched with cp.async), bf16
+//    out + lse.  Several splits: fp32 partials (o/l, lse) for the LSE merge.
 //  * Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 softmax and
 //    epilogue.  Every wait is bounded; nothing traps.
 #include <cuda.h>
@@ -60,20 +61,28 @@ constexpr int kD = SV_LATENT_DIM;
 constexpr int kDHalf = kD / 2;
 constexpr int kTileN = SV_PAGE_SIZE;  // KV rows per tile = one page
 constexpr int kMTile = 128;           // folded query rows per unit
-constexpr int kStages = 4;
-constexpr int kBoxBytes = 64 * 128;            // one TMA box: 64 rows x 64 bf16
-constexpr int kStageBytes = 4 * kBoxBytes;     // 64 rows x 256 bf16
-constexpr int kXRowBytes = 64 * 4 + 16;        // exchanged score row, padded
-constexpr int kXBufBytes = kMTile * kXRowBytes;
+constexpr int kOwnStages = 3;
+constexpr int kOthStages = 2;
+constexpr int kBoxBytes = 64 * 128;            // one KV TMA box: 64 rows x 64 bf16
+constexpr int kHalfTileBytes = 4 * kBoxBytes;  // 64 rows x 256 bf16
+constexpr int kQBoxBytes = 128 * 128;          // one Q TMA box: 128 rows x 64 bf16
+constexpr int kQHalfBytes = 4 * kQBoxBytes;    // 128 rows x 256 bf16
 constexpr int kThreads = 192;
 constexpr int kNumBars = 18;
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS = 384, kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // in log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
-constexpr int kSmemUsed = kStages * kStageBytes + 2 * kXBufBytes + kNumBars * 8 + 16;
+// shared memory map (offsets from the 1024-aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffOwn = kOffQ + kQHalfBytes;
+constexpr int kOffOth = kOffOwn + kOwnStages * kHalfTileBytes;
+constexpr int kOffBar = kOffOth + kOthStages * kHalfTileBytes;
+constexpr int kSmemUsed = kOffBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kMTile * kDHalf * 2 <= kOthStages * kHalfTileBytes,
+              "gate prefetch reuses the other-half ring");
 
 struct VerifyParams {
   const __nv_bfloat16* q;
@@ -101,10 +110,9 @@ __device__ __forceinline__ int load_bound(const VerifyParams& p, int tok) {
 }
 
 // Bounded wait taken by a whole warp; all lanes get the same answer.
-template <bool kCluster>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int32_t* status) {
-  const bool ok = mbar_wait<kCluster>(bar, parity, abort_flag, status);
+  const bool ok = mbar_wait<false>(bar, parity, abort_flag, status);
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
@@ -119,30 +127,31 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_verify_kernel(const __grid_constant__ CUtensorMap tmap_kv, const VerifyParams p) {
+    mla_verify_kernel(const __grid_constant__ CUtensorMap tmap_kv,
+                      const __grid_constant__ CUtensorMap tmap_q, const VerifyParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* const sptr = smem_raw + (sbase - raw);
-  const uint32_t stage0 = sbase;
-  const uint32_t xbuf0 = sbase + kStages * kStageBytes;
-  const uint32_t bar0 = xbuf0 + 2 * kXBufBytes;
-  auto kv_full = [&](int s) { return bar0 + 8u * s; };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (4 + s); };
-  auto s_full = [&](int b) { return bar0 + 8u * (8 + b); };
-  auto p_full = [&](int b) { return bar0 + 8u * (10 + b); };
-  auto pv_done = [&](int b) { return bar0 + 8u * (12 + b); };
-  auto xfull = [&](int b) { return bar0 + 8u * (14 + b); };
-  const uint32_t q_ready = bar0 + 8u * 16;
+  const uint32_t q_s = sbase + kOffQ;
+  const uint32_t own0 = sbase + kOffOwn;
+  const uint32_t oth0 = sbase + kOffOth;
+  const uint32_t bar0 = sbase + kOffBar;
+  auto own_full = [&](int s) { return bar0 + 8u * s; };
+  auto own_empty = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto oth_full = [&](int s) { return bar0 + 8u * (6 + s); };
+  auto oth_empty = [&](int s) { return bar0 + 8u * (8 + s); };
+  auto s_full = [&](int b) { return bar0 + 8u * (10 + b); };
+  auto p_full = [&](int b) { return bar0 + 8u * (12 + b); };
+  auto pv_done = [&](int b) { return bar0 + 8u * (14 + b); };
+  const uint32_t q_ready = bar0 + 8u * 16;  // Q own half in TMEM + Q other half in SMEM
   const uint32_t drain_bar = bar0 + 8u * 17;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sptr + (bar0 - sbase) + 8 * kNumBars);
-  volatile int* const abort_flag =
-      reinterpret_cast<volatile int*>(sptr + (bar0 - sbase) + 8 * kNumBars + 4);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sptr + kOffBar + 8 * kNumBars);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(sptr + kOffBar + 8 * kNumBars + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();
-  const uint32_t peer = crank ^ 1u;
+  const int half = blockIdx.x & 1;  // latent half of O owned by this CTA
   const int unit = blockIdx.x >> 1;
   const int S = p.num_splits;
   const int s_idx = unit % S;
@@ -166,17 +175,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = max(0, hi_eff - lo);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+    for (int s = 0; s < kOwnStages; ++s) {
+      mbar_init(own_full(s), 1);
+      mbar_init(own_empty(s), 1);
+    }
+    for (int s = 0; s < kOthStages; ++s) {
+      mbar_init(oth_full(s), 1);
+      mbar_init(oth_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
       mbar_init(p_full(b), 128);
       mbar_init(pv_done(b), 1);
-      mbar_init(xfull(b), 128);
     }
-    mbar_init(q_ready, 128);
+    mbar_init(q_ready, 128 + 1);  // 128 softmax threads (TMEM half) + the producer (TMA half)
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init_cluster();
@@ -189,98 +201,130 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  cluster_sync();  // the peer's barriers exist before any remote arrive
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ntiles > 0) {
       tma_prefetch_desc(&tmap_kv);
-      int last_round[kStages] = {-1, -1, -1, -1};
+      // the other latent half of this unit's 128 query rows (A of the SMEM score GEMM)
+      const int q_row0 = (int)((long long)r * Mq + m_tile * kMTile);
+      mbar_arrive_expect_tx(q_ready, kQHalfBytes);
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        tma_load_2d(q_s + b * kQBoxBytes, &tmap_q, q_ready, (1 - half) * kDHalf + b * 64, q_row0);
+      int last_own[kOwnStages] = {-1, -1, -1};
+      int last_oth[kOthStages] = {-1, -1};
       for (int it = 0; it < ntiles; ++it) {
-        const int st = it & (kStages - 1);
-        const int round = it / kStages;
-        if (round > 0 && !mbar_wait<false>(kv_empty(st), (round - 1) & 1, abort_flag, p.status))
-          break;
-        mbar_arrive_expect_tx(kv_full(st), kStageBytes);
         const int j = lo + it;
         int page = __ldg(p.block_table + (long long)r * p.max_pages + j);
         if (page < 0 || page >= p.num_pages) {
           if (p.status) atomicOr(p.status, SV_DEV_BAD_PAGE);
           page = 0;
         }
-        const uint32_t dst = stage0 + st * kStageBytes;
+        // own half: scores and P V
+        const int so = it % kOwnStages;
+        const int ro = it / kOwnStages;
+        if (ro > 0 && !mbar_wait<false>(own_empty(so), (ro - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(own_full(so), kHalfTileBytes);
 #pragma unroll
         for (int b = 0; b < 4; ++b)
-          tma_load_2d(dst + b * kBoxBytes, &tmap_kv, kv_full(st), (int)crank * kDHalf + b * 64,
-                      page * kTileN);
-        last_round[st] = round;
+          tma_load_2d(own0 + so * kHalfTileBytes + b * kBoxBytes, &tmap_kv, own_full(so),
+                      half * kDHalf + b * 64, page * kTileN);
+        last_own[so] = ro;
+        // other half: scores only
+        const int sx = it % kOthStages;
+        const int rx = it / kOthStages;
+        if (rx > 0 && !mbar_wait<false>(oth_empty(sx), (rx - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(oth_full(sx), kHalfTileBytes);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          tma_load_2d(oth0 + sx * kHalfTileBytes + b * kBoxBytes, &tmap_kv, oth_full(sx),
+                      (1 - half) * kDHalf + b * 64, page * kTileN);
+        last_oth[sx] = rx;
       }
       // every copy this CTA started has landed before teardown
-      for (int st = 0; st < kStages; ++st)
-        if (last_round[st] >= 0) drain_wait(kv_full(st), last_round[st] & 1);
+      drain_wait(q_ready, 0);
+      for (int s = 0; s < kOwnStages; ++s)
+        if (last_own[s] >= 0) drain_wait(own_full(s), last_own[s] & 1);
+      for (int s = 0; s < kOthStages; ++s)
+        if (last_oth[s] >= 0) drain_wait(oth_full(s), last_oth[s] & 1);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
-    bool ok = ntiles > 0 && warp_wait<false>(q_ready, 0, abort_flag, p.status);
+    bool ok = ntiles > 0 && warp_wait(q_ready, 0, abort_flag, p.status);
     bool issued = false;
     auto issue_pv = [&](int i) -> bool {
       const int sb = i & 1;
-      const int st = i & (kStages - 1);
-      if (!warp_wait<false>(p_full(sb), (i >> 1) & 1, abort_flag, p.status)) return false;
+      const int so = i % kOwnStages;
+      if (!warp_wait(p_full(sb), (i >> 1) & 1, abort_flag, p.status)) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t a = tmem + kTmemS + 64u * sb;
-        const uint32_t sa = stage0 + st * kStageBytes;
+        const uint32_t sa = own0 + so * kHalfTileBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          // B = V tile, MN-major: N = 256 latent columns in four 64-wide boxes
-          // (LBO = box stride), K = 16 KV rows per step (SBO = 8-row stride).
+          // B = V tile (own half), MN-major: N = 256 latent columns in four
+          // 64-wide boxes (LBO = box stride), K = 16 KV rows per step (SBO = 8-row stride).
           const uint64_t bd = sdesc_sw128(sa + kk * 16 * 128, kBoxBytes, 1024);
           mma_ts(tmem + kTmemO, a + 8u * kk, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(kv_empty(st));
+        mma_commit(own_empty(so));
         mma_commit(pv_done(sb));
       }
       __syncwarp();
       return true;
     };
+    auto zero_tail = [&](uint8_t* tile, int rows_valid) {
+      // rows no query row of this unit may see: zero them (pool slack may be NaN)
+      const int nrows = kTileN - rows_valid;
+      for (int idx = lane; idx < nrows * 4 * 8; idx += 32) {
+        const int c16 = idx & 7;
+        const int rr = (idx >> 3) % nrows;
+        const int b = (idx >> 3) / nrows;
+        *reinterpret_cast<uint4*>(tile + b * kBoxBytes + (rows_valid + rr) * 128 + c16 * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
     if (ok) tc_fence_after();
     for (int it = 0; ok && it < ntiles; ++it) {
-      const int st = it & (kStages - 1);
+      const int so = it % kOwnStages;
+      const int sx = it % kOthStages;
       const int sb = it & 1;
-      if (!warp_wait<false>(kv_full(st), (it / kStages) & 1, abort_flag, p.status)) {
+      if (!warp_wait(own_full(so), (it / kOwnStages) & 1, abort_flag, p.status) ||
+          !warp_wait(oth_full(sx), (it / kOthStages) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
       const int rows_valid = maxb_tile - (lo + it) * kTileN;
       if (rows_valid < kTileN) {
-        // rows no query row of this tile may see: zero them (pool slack may be NaN)
-        uint8_t* tile = sptr + (stage0 - sbase) + st * kStageBytes;
-        const int nrows = kTileN - rows_valid;
-        for (int idx = lane; idx < nrows * 4 * 8; idx += 32) {
-          const int c16 = idx & 7;
-          const int rr = (idx >> 3) % nrows;
-          const int b = (idx >> 3) / nrows;
-          *reinterpret_cast<uint4*>(tile + b * kBoxBytes + (rows_valid + rr) * 128 + c16 * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
+        zero_tail(sptr + kOffOwn + so * kHalfTileBytes, rows_valid);
+        zero_tail(sptr + kOffOth + sx * kHalfTileBytes, rows_valid);
         fence_proxy_async_smem();
         __syncwarp();
       }
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t sa = stage0 + st * kStageBytes;
+        const uint32_t ko = own0 + so * kHalfTileBytes;
+        const uint32_t kx = oth0 + sx * kHalfTileBytes;
         const uint32_t d = tmem + kTmemS + 64u * sb;
+        // B = K tile, K-major, 128-byte swizzle: step 16 latent columns (32
+        // bytes) inside a box, next box every 4 steps.
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          // B = K tile, K-major, 128-byte swizzle: step 16 latent columns
-          // (32 bytes) inside a box, next box every 4 steps.
-          const uint64_t bd = sdesc_sw128(sa + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(ko + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
           mma_ts(d, tmem + kTmemQ + 8u * kk, bd, idesc_s, kk > 0 ? 1u : 0u);
         }
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(q_s + (kk >> 2) * kQBoxBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(kx + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+          mma_ss(d, ad, bd, idesc_s, 1u);
+        }
         mma_commit(s_full(sb));
+        mma_commit(oth_empty(sx));
       }
       __syncwarp();
       issued = true;
@@ -308,17 +352,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (ntiles > 0) {
       // this CTA's half of the query row -> TMEM (bf16 pairs per 32-bit column)
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + row_g * kD + crank * kDHalf);
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + row_g * kD + half * kDHalf);
+      uint4 qv[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) qv[u] = valid ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const uint4 x = valid ? __ldg(src + c * 8 + u) : make_uint4(0u, 0u, 0u, 0u);
-          v[4 * u + 0] = x.x;
-          v[4 * u + 1] = x.y;
-          v[4 * u + 2] = x.z;
-          v[4 * u + 3] = x.w;
+          v[4 * u + 0] = qv[8 * c + u].x;
+          v[4 * u + 1] = qv[8 * c + u].y;
+          v[4 * u + 2] = qv[8 * c + u].z;
+          v[4 * u + 3] = qv[8 * c + u].w;
         }
         tmem_st32(tmem + lane_off + kTmemQ + 32u * c, v);
       }
@@ -329,15 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     float m_ref = -INFINITY;  // running max (log2 units) used for exponentiation
     float l_sum = 0.f;
-    const uint32_t my_x = xbuf0 + (uint32_t)i * kXRowBytes;
-    const uint32_t peer_x = mapa_shared(my_x, peer);
-    const uint32_t peer_xfull0 = mapa_shared(xfull(0), peer);
-    const uint32_t peer_xfull1 = mapa_shared(xfull(1), peer);
     bool ok = true;
     for (int it = 0; it < ntiles; ++it) {
       const int sb = it & 1;
       const uint32_t par = (it >> 1) & 1;
-      if (!warp_wait<false>(s_full(sb), par, abort_flag, p.status)) { ok = false; break; }
+      if (!warp_wait(s_full(sb), par, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       float x[64];
       {
@@ -351,33 +393,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[32 + c] = __uint_as_float(b[c]);
         }
       }
-      // swap partial scores with the peer CTA (other latent half)
-      const uint32_t dst = peer_x + (uint32_t)sb * kXBufBytes;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_cluster_v4(dst + 16u * c, x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
-      mbar_arrive_cluster(sb ? peer_xfull1 : peer_xfull0);
-      if (!warp_wait<true>(xfull(sb), par, abort_flag, p.status)) { ok = false; break; }
-      const float4* theirs =
-          reinterpret_cast<const float4*>(sptr + (my_x - sbase) + (uint32_t)sb * kXBufBytes);
       const int lim = b_i - (lo + it) * kTileN;  // columns >= lim are masked
       float tmax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 y = theirs[c];
-        float v0 = (x[4 * c + 0] + y.x) * p.scale_log2;
-        float v1 = (x[4 * c + 1] + y.y) * p.scale_log2;
-        float v2 = (x[4 * c + 2] + y.z) * p.scale_log2;
-        float v3 = (x[4 * c + 3] + y.w) * p.scale_log2;
-        if (4 * c + 0 >= lim) v0 = -INFINITY;
-        if (4 * c + 1 >= lim) v1 = -INFINITY;
-        if (4 * c + 2 >= lim) v2 = -INFINITY;
-        if (4 * c + 3 >= lim) v3 = -INFINITY;
-        x[4 * c + 0] = v0;
-        x[4 * c + 1] = v1;
-        x[4 * c + 2] = v2;
-        x[4 * c + 3] = v3;
-        tmax = fmaxf(tmax, fmaxf(fmaxf(v0, v1), fmaxf(v2, v3)));
+      for (int c = 0; c < 64; ++c) {
+        const float v = (c < lim) ? x[c] * p.scale_log2 : -INFINITY;
+        x[c] = v;
+        tmax = fmaxf(tmax, v);
       }
       // lazy rescale: move the reference max only when it grows by > 2^8
       const bool move = tmax > m_ref + kRescaleThreshold;
@@ -386,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = rescale_o ? exp2f(m_ref - m_new) : 1.0f;
       if (__any_sync(0xFFFFFFFFu, rescale_o)) {
         // O holds tiles < it: wait for PV(it-1), then scale the row in TMEM
-        if (!warp_wait<false>(pv_done((it - 1) & 1), ((it - 1) >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait(pv_done((it - 1) & 1), ((it - 1) >> 1) & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
@@ -422,16 +444,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- epilogue
+    const bool fused_gate = (S == 1);
     if (ok && ntiles > 0)
-      ok = warp_wait<false>(pv_done((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag,
-                            p.status);
+      ok = warp_wait(pv_done((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
     tc_fence_after();
+    // the other-half ring is idle once the last P V has completed: stage the gate there
+    const uint32_t gate_s = oth0 + (uint32_t)i * (kDHalf * 2);
+    if (fused_gate && valid) {
+      const __nv_bfloat16* gsrc = p.gate + row_g * kD + half * kDHalf;
+#pragma unroll
+      for (int u = 0; u < 32; ++u) cp_async_16(gate_s + 16u * u, gsrc + 8 * u);
+      cp_async_commit();
+    }
     const bool have_o = ok && ntiles > 0;
     const float inv_l = (l_sum > 0.f) ? 1.0f / l_sum : 0.f;
     const float lse_v = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
-    if (S == 1) {
-      const uint4* g = reinterpret_cast<const uint4*>(p.gate + row_g * kD + crank * kDHalf);
-      uint4* o = reinterpret_cast<uint4*>(p.out + row_g * kD + crank * kDHalf);
+    if (fused_gate) {
+      if (valid) cp_async_wait_all();
+      const uint4* g = reinterpret_cast<const uint4*>(sptr + (gate_s - sbase));
+      uint4* o = reinterpret_cast<uint4*>(p.out + row_g * kD + half * kDHalf);
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t v[32];
@@ -445,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint4 graw = __ldg(g + 4 * c + u);
+            const uint4 graw = g[4 * c + u];
             const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
             uint32_t ow[4];
 #pragma unroll
@@ -459,10 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (valid && crank == 0) p.lse[row_g] = lse_v;
+      if (valid && half == 0) p.lse[row_g] = lse_v;
     } else {
       float4* po = reinterpret_cast<float4*>(p.part_o + ((long long)s_idx * p.rows_total + row_g) * kD +
-                                             crank * kDHalf);
+                                             half * kDHalf);
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t v[32];
@@ -482,18 +513,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         __uint_as_float(v[4 * u + 3]) * inv_l);
         }
       }
-      if (valid && crank == 0) p.part_lse[(long long)s_idx * p.rows_total + row_g] = lse_v;
+      if (valid && half == 0) p.part_lse[(long long)s_idx * p.rows_total + row_g] = lse_v;
     }
   }
 
-  // ---- teardown
+  // ---- teardown (every warp is converged here)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  cluster_sync();  // neither CTA leaves while the peer may still touch its SMEM
 }
 
 // ------------------------------------------------------------------ host side
@@ -509,6 +539,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
   });
   return fn;
+}
+
+// 2-D tensor map over a [rows][512] bf16 matrix, boxes of box_rows x 64 columns.
+bool encode_2d(CUtensorMap* map, const void* base, long long rows, int box_rows) {
+  auto encode = get_encode_fn();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 constexpr int kMaxDevices = 64;
@@ -533,11 +577,13 @@ bool device_setup(int* sm_count) {
   return true;
 }
 
+// Splits: enough (request, row tile, split, latent half) CTAs to fill the SMs
+// once, each split keeping at least 4 KV tiles.
 int auto_splits(int R, int q_per_req, int H, int max_pages, int sm_count) {
   const long long n_mt = ((long long)H * q_per_req + kMTile - 1) / kMTile;
-  const long long pairs = (long long)R * n_mt;
-  if (pairs <= 0) return 1;
-  long long s = (long long)sm_count / (2 * pairs);
+  const long long ctas = 2ll * R * n_mt;
+  if (ctas <= 0) return 1;
+  long long s = (long long)sm_count / ctas;
   const long long by_len = max_pages / 4;
   if (s > by_len) s = by_len;
   if (s > SV_MAX_SPLITS) s = SV_MAX_SPLITS;
@@ -545,7 +591,9 @@ int auto_splits(int R, int q_per_req, int H, int max_pages, int sm_count) {
   return (int)s;
 }
 
-inline bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
+inline bool misaligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0;
+}
 
 }  // namespace
 }  // namespace sv
@@ -582,7 +630,7 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
   if (num_splits < 0 || num_splits > SV_MAX_SPLITS) return SV_ERR_SHAPE;
   const long long T = (long long)R * q_per_req;
   if (T == 0) return SV_OK;
-  if (T * H > (1ll << 40) || (long long)num_pages * kTileN > 0x7FFFFFFFll) return SV_ERR_SHAPE;
+  if (T * H > 0x7FFFFFFFll || (long long)num_pages * kTileN > 0x7FFFFFFFll) return SV_ERR_SHAPE;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return SV_ERR_SHAPE;
   if (num_pages < 1 || max_pages_per_req < 1) return SV_ERR_SHAPE;
   if (!q_latent || !kv_pages || !block_table || !kv_bounds || !gate || !out || !lse)
@@ -604,17 +652,10 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
     part_o = static_cast<float*>(workspace);
     part_lse = part_o + (size_t)S * T * H * kD;
   }
-  auto encode = get_encode_fn();
-  if (!encode) return SV_ERR_DEVICE;
-  CUtensorMap tmap;
-  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)num_pages * kTileN};
-  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  const cuuint32_t box[2] = {64, 64};
-  const cuuint32_t estr[2] = {1, 1};
-  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_pages), dims,
-             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return SV_ERR_ALIGN;
+  if (!get_encode_fn()) return SV_ERR_DEVICE;
+  CUtensorMap tmap_kv, tmap_q;
+  if (!encode_2d(&tmap_kv, kv_pages, (long long)num_pages * kTileN, kTileN)) return SV_ERR_ALIGN;
+  if (!encode_2d(&tmap_q, q_latent, T * H, kMTile)) return SV_ERR_ALIGN;
 
   VerifyParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q_latent);
@@ -636,24 +677,11 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
   prm.n_mtiles = (int)(((long long)H * q_per_req + kMTile - 1) / kMTile);
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
 
-  const long long units = (long long)R * prm.n_mtiles * S;
-  if (2 * units > 0x7FFFFFFFll) return SV_ERR_SHAPE;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(2 * units), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, mla_verify_kernel, tmap, prm) != cudaSuccess) {
-    cudaGetLastError();
-    return SV_ERR_LAUNCH;
-  }
+  const long long ctas = 2ll * R * prm.n_mtiles * S;
+  if (ctas > 0x7FFFFFFFll) return SV_ERR_SHAPE;
+  mla_verify_kernel<<<(unsigned)ctas, kThreads, kSmemBytes,
+                      reinterpret_cast<cudaStream_t>(stream)>>>(tmap_kv, tmap_q, prm);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_LAUNCH;
   if (S > 1) {
     if (launch_lse_combine(part_o, part_lse, S, T * H, gate, out, lse,
                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
