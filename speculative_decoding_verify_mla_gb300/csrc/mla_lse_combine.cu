@@ -9,30 +9,40 @@
 // an empty partial is exactly 0 and its o_s is never read, so a zero-bound
 // row cannot poison the merge with 0 * NaN.
 //
-// HBM-bound: one warp per (token, head) row; each lane owns 16 of the 512
-// columns as four float4 (coalesced 512-byte warp accesses per split), the
-// gate and the output move as 8-byte bf16x4 accesses.
+// HBM-bound: one warp per half row (256 of the 512 columns); each lane owns
+// two float4 of every split (coalesced 512-byte warp accesses), the loads of
+// eight splits are in flight before their FMAs, and the gate and the output
+// move as 8-byte bf16x4 accesses.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
-#include "specverify.h"
+#include "sv_ptx.cuh"
 
 namespace sv {
 namespace {
 
 constexpr int kCombineThreads = 256;
 
-__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
-
 __global__ void __launch_bounds__(kCombineThreads)
     lse_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                        int S, long long rows, const __nv_bfloat16* __restrict__ gate,
                        __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
+  // one warp per half row (256 columns): lane owns columns 128j + 4 lane .. +3, j = 0, 1
   const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
-  if (row >= rows) return;
+  const long long hrow = (long long)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
+  if (hrow >= 2 * rows) return;
+  const long long row = hrow >> 1;
+  const int col0 = (int)(hrow & 1) * 256 + 4 * lane;
+  // the gate does not depend on the attention kernel: fetch it first
+  uint2 graw[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+    graw[j] = __ldg(reinterpret_cast<const uint2*>(gate + row * 512 + col0 + 128 * j));
+  // when launched behind the attention kernel (programmatic dependent
+  // launch), wait here until its partials are complete and visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // split weights: lane s holds lse_s for s = lane and lane + 32
   float l0 = -INFINITY, l1 = -INFINITY;
@@ -42,9 +52,7 @@ __global__ void __launch_bounds__(kCombineThreads)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
 
-  float4 acc[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
   float lse_row = -INFINITY;
   if (m != -INFINITY) {
     const float w0 = (l0 == -INFINITY) ? 0.f : __expf(l0 - m);
@@ -54,35 +62,44 @@ __global__ void __launch_bounds__(kCombineThreads)
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
     const float inv_z = 1.0f / z;
     lse_row = m + __logf(z);
-    for (int s = 0; s < S; ++s) {
-      const float ws = __shfl_sync(0xFFFFFFFFu, s < 32 ? w0 : w1, s & 31) * inv_z;
-      if (ws == 0.f) continue;  // warp-uniform: an empty or negligible split is never read
-      const float4* src = reinterpret_cast<const float4*>(part_o + ((long long)s * rows + row) * 512);
+    // eight splits per round: all their loads are in flight before any FMA
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float4 v[8][2];
+      float ws[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 v = __ldcs(src + lane + 32 * j);
-        acc[j].x = fmaf(ws, v.x, acc[j].x);
-        acc[j].y = fmaf(ws, v.y, acc[j].y);
-        acc[j].z = fmaf(ws, v.z, acc[j].z);
-        acc[j].w = fmaf(ws, v.w, acc[j].w);
+      for (int u = 0; u < 8; ++u) {
+        const int s = s0 + u;
+        ws[u] = (s < S) ? __shfl_sync(0xFFFFFFFFu, s < 32 ? w0 : w1, s & 31) * inv_z : 0.f;
+        const float* src = part_o + ((long long)min(s, S - 1) * rows + row) * 512 + col0;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          v[u][j] = (ws[u] != 0.f) ? __ldcs(reinterpret_cast<const float4*>(src + 128 * j))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          acc[j].x = fmaf(ws[u], v[u][j].x, acc[j].x);
+          acc[j].y = fmaf(ws[u], v[u][j].y, acc[j].y);
+          acc[j].z = fmaf(ws[u], v[u][j].z, acc[j].z);
+          acc[j].w = fmaf(ws[u], v[u][j].w, acc[j].w);
+        }
       }
     }
   }
-  const uint2* g2 = reinterpret_cast<const uint2*>(gate + row * 512);
-  uint2* o2 = reinterpret_cast<uint2*>(out + row * 512);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint2 graw = __ldg(g2 + lane + 32 * j);
-    const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.x));
-    const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.y));
-    const __nv_bfloat162 r0 = __floats2bfloat162_rn(sigmoidf_(ga.x) * acc[j].x, sigmoidf_(ga.y) * acc[j].y);
-    const __nv_bfloat162 r1 = __floats2bfloat162_rn(sigmoidf_(gb.x) * acc[j].z, sigmoidf_(gb.y) * acc[j].w);
+  for (int j = 0; j < 2; ++j) {
+    const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw[j].x));
+    const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw[j].y));
+    const __nv_bfloat162 r0 = __floats2bfloat162_rn(fast_sigmoid(ga.x) * acc[j].x, fast_sigmoid(ga.y) * acc[j].y);
+    const __nv_bfloat162 r1 = __floats2bfloat162_rn(fast_sigmoid(gb.x) * acc[j].z, fast_sigmoid(gb.y) * acc[j].w);
     uint2 packed;
     packed.x = *reinterpret_cast<const uint32_t*>(&r0);
     packed.y = *reinterpret_cast<const uint32_t*>(&r1);
-    o2[lane + 32 * j] = packed;
+    *reinterpret_cast<uint2*>(out + row * 512 + col0 + 128 * j) = packed;
   }
-  if (lane == 0) lse_out[row] = lse_row;
+  if (lane == 0 && (hrow & 1) == 0) lse_out[row] = lse_row;
 }
 
 }  // namespace
@@ -91,11 +108,24 @@ __global__ void __launch_bounds__(kCombineThreads)
 cudaError_t launch_lse_combine(const float* part_o, const float* part_lse, int S, long long rows,
                                const void* gate, void* out, float* lse, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  const long long blocks = (rows + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
-  lse_combine_kernel<<<(unsigned)blocks, kCombineThreads, 0, stream>>>(
-      part_o, part_lse, S, rows, static_cast<const __nv_bfloat16*>(gate),
-      static_cast<__nv_bfloat16*>(out), lse);
-  return cudaGetLastError();
+  const long long blocks = (2 * rows + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
+  // programmatic dependent launch: the grid may start while the previous
+  // kernel on the stream finishes; griddepcontrol.wait guards the partials
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(kCombineThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, lse_combine_kernel, part_o, part_lse, S, rows,
+                                           static_cast<const __nv_bfloat16*>(gate),
+                                           static_cast<__nv_bfloat16*>(out), lse);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e;
 }
 
 }  // namespace sv

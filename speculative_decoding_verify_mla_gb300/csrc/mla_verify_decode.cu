@@ -68,7 +68,8 @@ constexpr int kHalfTileBytes = 4 * kBoxBytes;  // 64 rows x 256 bf16
 constexpr int kQBoxBytes = 128 * 128;          // one Q TMA box: 128 rows x 64 bf16
 constexpr int kQHalfBytes = 4 * kQBoxBytes;    // 128 rows x 256 bf16
 constexpr int kThreads = 192;
-constexpr int kNumBars = 18;
+constexpr int kNumBars = 19;
+constexpr uint32_t kEpilogueBarId = 1;  // named barrier of the softmax warps
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS = 384, kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // in log2 units
 constexpr float kLn2 = 0.6931471805599453f;
@@ -81,8 +82,9 @@ constexpr int kOffBar = kOffOth + kOthStages * kHalfTileBytes;
 constexpr int kSmemUsed = kOffBar + kNumBars * 8 + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kMTile * kDHalf * 2 <= kOthStages * kHalfTileBytes,
-              "gate prefetch reuses the other-half ring");
+static_assert(kOffOth == kOffOwn + kOwnStages * kHalfTileBytes &&
+                  kOwnStages * kHalfTileBytes + kOthStages * kHalfTileBytes >= 8 * kQBoxBytes,
+              "the epilogue stages a 128 x 256 fp32 tile over the two KV rings");
 
 struct VerifyParams {
   const __nv_bfloat16* q;
@@ -124,11 +126,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + __expf(-g)); }
-
+// Tensor maps: tmap_kv 2-D over the page pool [pages*64][512] bf16; tmap_q,
+// tmap_gate, tmap_out 3-D [R][M][512] bf16 (rows past a request's M fall out
+// of bounds: zero on load, dropped on store); tmap_part 4-D [S][R][M][512] fp32.
 __global__ void __launch_bounds__(kThreads, 1)
     mla_verify_kernel(const __grid_constant__ CUtensorMap tmap_kv,
-                      const __grid_constant__ CUtensorMap tmap_q, const VerifyParams p) {
+                      const __grid_constant__ CUtensorMap tmap_q,
+                      const __grid_constant__ CUtensorMap tmap_gate,
+                      const __grid_constant__ CUtensorMap tmap_out,
+                      const __grid_constant__ CUtensorMap tmap_part, const VerifyParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -146,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto pv_done = [&](int b) { return bar0 + 8u * (14 + b); };
   const uint32_t q_ready = bar0 + 8u * 16;  // Q own half in TMEM + Q other half in SMEM
   const uint32_t drain_bar = bar0 + 8u * 17;
+  const uint32_t gate_full = bar0 + 8u * 18;  // gate tile staged in the Q region
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sptr + kOffBar + 8 * kNumBars);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(sptr + kOffBar + 8 * kNumBars + 4);
 
@@ -159,6 +166,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_tile = rm % p.n_mtiles;
   const int r = rm / p.n_mtiles;
   const int Mq = p.H * p.q_per_req;
+
+  // softmax warps: start fetching this CTA's half of their query row now, so
+  // the load overlaps the set-up below (row i of the tile <-> TMEM lane i)
+  uint4 qv[32];
+  if (warp >= 2) {
+    const int f0 = m_tile * kMTile + (warp & 3) * 32 + lane;
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((long long)r * Mq + f0) * kD + half * kDHalf);
+#pragma unroll
+    for (int u = 0; u < 32; ++u) qv[u] = (f0 < Mq) ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+  }
 
   // ---- unit geometry (every thread derives the same values)
   int maxb_req = 0;
@@ -190,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(q_ready, 128 + 1);  // 128 softmax threads (TMEM half) + the producer (TMA half)
     mbar_init(drain_bar, 1);
+    mbar_init(gate_full, 1);
     *abort_flag = 0;
     fence_mbar_init_cluster();
   }
@@ -207,11 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && ntiles > 0) {
       tma_prefetch_desc(&tmap_kv);
       // the other latent half of this unit's 128 query rows (A of the SMEM score GEMM)
-      const int q_row0 = (int)((long long)r * Mq + m_tile * kMTile);
       mbar_arrive_expect_tx(q_ready, kQHalfBytes);
 #pragma unroll
       for (int b = 0; b < 4; ++b)
-        tma_load_2d(q_s + b * kQBoxBytes, &tmap_q, q_ready, (1 - half) * kDHalf + b * 64, q_row0);
+        tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_ready, (1 - half) * kDHalf + b * 64,
+                    m_tile * kMTile, r);
       int last_own[kOwnStages] = {-1, -1, -1};
       int last_oth[kOthStages] = {-1, -1};
       for (int it = 0; it < ntiles; ++it) {
@@ -343,19 +361,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax + epilogue
     const int wq = warp & 3;  // TMEM lane quadrant of this warp
     const int i = wq * 32 + lane;
+    const bool leader = (warp == 2 && lane == 0);
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const int f = m_tile * kMTile + i;
     const bool valid = f < Mq;
     const int t_loc = valid ? f / p.H : 0;
     const long long row_g = (long long)r * Mq + f;
     const int b_i = valid ? load_bound(p, r * p.q_per_req + t_loc) : 0;
+    const bool fused_gate = (S == 1);
 
     if (ntiles > 0) {
       // this CTA's half of the query row -> TMEM (bf16 pairs per 32-bit column)
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + row_g * kD + half * kDHalf);
-      uint4 qv[32];
-#pragma unroll
-      for (int u = 0; u < 32; ++u) qv[u] = valid ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
@@ -372,6 +388,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(q_ready);
     }
+    // Stage the gate tile (128 rows x 256 columns) into the Q region once no
+    // score GEMM will read it again.
+    auto load_gate = [&]() {
+      mbar_arrive_expect_tx(gate_full, kQHalfBytes);
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        tma_load_3d(q_s + b * kQBoxBytes, &tmap_gate, gate_full, half * kDHalf + b * 64,
+                    m_tile * kMTile, r);
+    };
+    if (fused_gate && ntiles == 0 && leader) load_gate();
 
     float m_ref = -INFINITY;  // running max (log2 units) used for exponentiation
     float l_sum = 0.f;
@@ -380,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sb = it & 1;
       const uint32_t par = (it >> 1) & 1;
       if (!warp_wait(s_full(sb), par, abort_flag, p.status)) { ok = false; break; }
+      if (fused_gate && it == ntiles - 1 && leader) load_gate();  // last score GEMM is done
       tc_fence_after();
       float x[64];
       {
@@ -431,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float psum = 0.f;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = exp2f(x[2 * c] - msub);
-        const float p1 = exp2f(x[2 * c + 1] - msub);
+        const float p0 = fast_exp2(x[2 * c] - msub);
+        const float p1 = fast_exp2(x[2 * c + 1] - msub);
         psum += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
@@ -443,26 +470,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(p_full(sb));
     }
 
-    // ---- epilogue
-    const bool fused_gate = (S == 1);
+    // ---- epilogue: O/l (gated bf16, or fp32 partial) staged swizzled in SMEM,
+    // then written with TMA tensor stores (coalesced; rows past M are dropped)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // a dependent merge may launch
     if (ok && ntiles > 0)
       ok = warp_wait(pv_done((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
     tc_fence_after();
-    // the other-half ring is idle once the last P V has completed: stage the gate there
-    const uint32_t gate_s = oth0 + (uint32_t)i * (kDHalf * 2);
-    if (fused_gate && valid) {
-      const __nv_bfloat16* gsrc = p.gate + row_g * kD + half * kDHalf;
-#pragma unroll
-      for (int u = 0; u < 32; ++u) cp_async_16(gate_s + 16u * u, gsrc + 8 * u);
-      cp_async_commit();
-    }
     const bool have_o = ok && ntiles > 0;
     const float inv_l = (l_sum > 0.f) ? 1.0f / l_sum : 0.f;
     const float lse_v = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
+    // staging: the KV rings are idle once the last P V has completed
+    uint8_t* const stage = sptr + kOffOwn;
+    const uint32_t row_off = (uint32_t)i * 128u;
+    const uint32_t swz = (uint32_t)(i & 7);
     if (fused_gate) {
-      if (valid) cp_async_wait_all();
-      const uint4* g = reinterpret_cast<const uint4*>(sptr + (gate_s - sbase));
-      uint4* o = reinterpret_cast<uint4*>(p.out + row_g * kD + half * kDHalf);
+      const bool gate_ok = warp_wait(gate_full, 0, abort_flag, p.status);
+      const uint8_t* const gs = sptr + kOffQ;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t v[32];
@@ -473,27 +496,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 32; ++u) v[u] = 0u;
         }
-        if (valid) {
+        // columns 32c .. 32c+31 of this half: box c/2, 16-byte chunks (c%2)*4 + u
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint4 graw = g[4 * c + u];
-            const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
-            uint32_t ow[4];
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t off = (uint32_t)(c >> 1) * kQBoxBytes + row_off +
+                               (((uint32_t)((c & 1) * 4 + u) ^ swz) << 4);
+          uint4 graw = gate_ok ? *reinterpret_cast<const uint4*>(gs + off) : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
+          uint32_t ow[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
-              const float o0 = __uint_as_float(v[8 * u + 2 * e]) * inv_l * sigmoidf_(gf.x);
-              const float o1 = __uint_as_float(v[8 * u + 2 * e + 1]) * inv_l * sigmoidf_(gf.y);
-              ow[e] = pack_bf16x2(o0, o1);
-            }
-            o[4 * c + u] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+          for (int e = 0; e < 4; ++e) {
+            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+            const float o0 = __uint_as_float(v[8 * u + 2 * e]) * inv_l * fast_sigmoid(gf.x);
+            const float o1 = __uint_as_float(v[8 * u + 2 * e + 1]) * inv_l * fast_sigmoid(gf.y);
+            ow[e] = pack_bf16x2(o0, o1);
           }
+          *reinterpret_cast<uint4*>(stage + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
         }
       }
       if (valid && half == 0) p.lse[row_g] = lse_v;
     } else {
-      float4* po = reinterpret_cast<float4*>(p.part_o + ((long long)s_idx * p.rows_total + row_g) * kD +
-                                             half * kDHalf);
+      // fp32: 32 columns per 128-byte box row; columns 32c .. 32c+31 are box c
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t v[32];
@@ -504,17 +527,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 32; ++u) v[u] = 0u;
         }
-        if (valid) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            po[8 * c + u] = make_float4(__uint_as_float(v[4 * u]) * inv_l,
-                                        __uint_as_float(v[4 * u + 1]) * inv_l,
-                                        __uint_as_float(v[4 * u + 2]) * inv_l,
-                                        __uint_as_float(v[4 * u + 3]) * inv_l);
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t off = (uint32_t)c * kQBoxBytes + row_off + (((uint32_t)u ^ swz) << 4);
+          *reinterpret_cast<float4*>(stage + off) =
+              make_float4(__uint_as_float(v[4 * u]) * inv_l, __uint_as_float(v[4 * u + 1]) * inv_l,
+                          __uint_as_float(v[4 * u + 2]) * inv_l, __uint_as_float(v[4 * u + 3]) * inv_l);
         }
       }
       if (valid && half == 0) p.part_lse[(long long)s_idx * p.rows_total + row_g] = lse_v;
     }
+    fence_proxy_async_smem();
+    named_bar_sync(kEpilogueBarId, 128);
+    if (leader) {
+      const uint32_t st0 = sbase + kOffOwn;
+      if (fused_gate) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          tma_store_3d(&tmap_out, st0 + b * kQBoxBytes, half * kDHalf + b * 64, m_tile * kMTile, r);
+      } else {
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+          tma_store_4d(&tmap_part, st0 + b * kQBoxBytes, half * kDHalf + b * 32, m_tile * kMTile, r,
+                       s_idx);
+      }
+      tma_store_commit();
+      tma_store_wait_read();  // SMEM stays valid until the stores have read it
+    }
+    __syncwarp();
   }
 
   // ---- teardown (every warp is converged here)
@@ -541,16 +581,21 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 2-D tensor map over a [rows][512] bf16 matrix, boxes of box_rows x 64 columns.
-bool encode_2d(CUtensorMap* map, const void* base, long long rows, int box_rows) {
+// Tiled tensor map with 128-byte swizzle over a row-major tensor whose
+// innermost dimension is the 512-wide latent row.
+bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base,
+                int rank, const cuuint64_t* dims, const cuuint32_t* box) {
   auto encode = get_encode_fn();
   if (!encode) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  cuuint64_t strides[4];
+  cuuint64_t acc = (cuuint64_t)elem_bytes;
+  for (int d = 0; d + 1 < rank; ++d) {
+    acc *= dims[d];
+    strides[d] = acc;
+  }
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return encode(map, dtype, rank, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -653,9 +698,28 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
     part_lse = part_o + (size_t)S * T * H * kD;
   }
   if (!get_encode_fn()) return SV_ERR_DEVICE;
-  CUtensorMap tmap_kv, tmap_q;
-  if (!encode_2d(&tmap_kv, kv_pages, (long long)num_pages * kTileN, kTileN)) return SV_ERR_ALIGN;
-  if (!encode_2d(&tmap_q, q_latent, T * H, kMTile)) return SV_ERR_ALIGN;
+  const long long Mq = (long long)H * q_per_req;
+  CUtensorMap tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part;
+  {
+    const cuuint64_t kv_dims[2] = {(cuuint64_t)kD, (cuuint64_t)num_pages * kTileN};
+    const cuuint32_t kv_box[2] = {64, (cuuint32_t)kTileN};
+    const cuuint64_t row_dims[3] = {(cuuint64_t)kD, (cuuint64_t)Mq, (cuuint64_t)R};
+    const cuuint32_t row_box[3] = {64, (cuuint32_t)kMTile, 1};
+    const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!encode_map(&tmap_kv, bf16, 2, kv_pages, 2, kv_dims, kv_box) ||
+        !encode_map(&tmap_q, bf16, 2, q_latent, 3, row_dims, row_box) ||
+        !encode_map(&tmap_gate, bf16, 2, gate, 3, row_dims, row_box) ||
+        !encode_map(&tmap_out, bf16, 2, out, 3, row_dims, row_box))
+      return SV_ERR_ALIGN;
+    if (S > 1) {
+      const cuuint64_t part_dims[4] = {(cuuint64_t)kD, (cuuint64_t)Mq, (cuuint64_t)R, (cuuint64_t)S};
+      const cuuint32_t part_box[4] = {32, (cuuint32_t)kMTile, 1, 1};
+      if (!encode_map(&tmap_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, part_o, 4, part_dims, part_box))
+        return SV_ERR_ALIGN;
+    } else {
+      tmap_part = tmap_out;  // unused with one split
+    }
+  }
 
   VerifyParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q_latent);
@@ -680,7 +744,8 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
   const long long ctas = 2ll * R * prm.n_mtiles * S;
   if (ctas > 0x7FFFFFFFll) return SV_ERR_SHAPE;
   mla_verify_kernel<<<(unsigned)ctas, kThreads, kSmemBytes,
-                      reinterpret_cast<cudaStream_t>(stream)>>>(tmap_kv, tmap_q, prm);
+                      reinterpret_cast<cudaStream_t>(stream)>>>(tmap_kv, tmap_q, tmap_gate, tmap_out,
+                                                                tmap_part, prm);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_LAUNCH;
   if (S > 1) {
     if (launch_lse_combine(part_o, part_lse, S, T * H, gate, out, lse,

@@ -113,22 +113,24 @@ __global__ void __launch_bounds__(kGreedyThreads)
   __syncthreads();
   if (!s_last) return;
 
-  // ---- last CTA: per-row argmax, then acceptance and trim per request
+  // ---- last CTA: per-row argmax (one warp per row), then acceptance and trim
   __threadfence();
-  for (int tt = tid; tt < T; tt += kGreedyThreads) {
+  const int lane = tid & 31;
+  for (int tt = tid >> 5; tt < T; tt += kGreedyThreads / 32) {
     unsigned long long best = 0ull;
     const unsigned long long* kr = keys + (long long)tt * nchunks;
-    for (int j = 0; j < nchunks; ++j) {
+    for (int j = lane; j < nchunks; j += 32) {
       const unsigned long long x = __ldcg(kr + j);
       best = x > best ? x : best;
     }
-    argmax_ids[tt] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+    best = warp_max_u64(best);
+    if (lane == 0) argmax_ids[tt] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
   }
   __syncthreads();
   for (int r = tid; r < R; r += kGreedyThreads) {
     const int base = r * (k + 1);
     int n = 0;
-    while (n < k && __ldcg(draft_tokens + (long long)r * k + n) == argmax_ids[base + n]) ++n;
+    while (n < k && __ldg(draft_tokens + (long long)r * k + n) == argmax_ids[base + n]) ++n;
     accepted[r] = n;
     next_tokens[r] = argmax_ids[base + n];
     kv_lens_out[r] = kv_lens_in[r] - (k - n);
@@ -140,9 +142,9 @@ __global__ void __launch_bounds__(kGreedyThreads)
 // workspace query and the launch agree.
 int greedy_chunk(int T, int V) {
   const long long total = (long long)T * V;
-  long long c = (total + 8 * 152 - 1) / (8 * 152);
-  c = (c + 2047) / 2048 * 2048;
-  if (c < 2048) c = 2048;
+  long long c = (total + 2 * 152 - 1) / (2 * 152);  // about two CTAs per SM
+  c = (c + 4095) / 4096 * 4096;
+  if (c < 4096) c = 4096;
   if (c > 32768) c = 32768;
   return (int)c;
 }

@@ -7,10 +7,14 @@ from . import binding as B
 
 
 class VerifyStep:
-    """Runs mla_verify_decode then spec_verify_greedy on one stream.
+    """Runs mla_verify_decode and spec_verify_greedy for one batch.
 
-    Output buffers and both workspaces are allocated once (torch) and reused,
-    so a step enqueues exactly the library's kernels and nothing else."""
+    The two parts are independent (the greedy verify reads the target logits,
+    not the attention output), so the greedy kernel runs on a side stream
+    forked from and joined back into the caller's stream: the step costs
+    about max(attention, greedy) instead of their sum.  Output buffers and
+    both workspaces are allocated once (torch) and reused, so a step enqueues
+    exactly the library's kernels and nothing else."""
 
     def __init__(self, device, R: int, k: int, H: int, V: int, max_pages: int,
                  num_splits: int = 0):
@@ -32,15 +36,21 @@ class VerifyStep:
         self.accepted = torch.empty(R, dtype=torch.int32, device=device)
         self.next_tokens = torch.empty(R, dtype=torch.int32, device=device)
         self.kv_lens_out = torch.empty(R, dtype=torch.int32, device=device)
+        self.side = torch.cuda.Stream(device=device)
 
     def __call__(self, q_latent, kv_pages, block_table, kv_bounds, gate, softmax_scale,
                  logits, draft_tokens, kv_lens_in):
+        main = torch.cuda.current_stream(self.device)
+        self.side.wait_stream(main)
+        with torch.cuda.stream(self.side):
+            B.spec_verify_greedy(logits, draft_tokens, kv_lens_in, self.k,
+                                 workspace=self.greedy_ws, argmax_ids=self.argmax,
+                                 accepted=self.accepted, next_tokens=self.next_tokens,
+                                 kv_lens_out=self.kv_lens_out)
         B.mla_verify_decode(q_latent, kv_pages, block_table, kv_bounds, gate, self.k + 1,
                             softmax_scale, num_splits=self.num_splits, workspace=self.attn_ws,
                             out=self.out, lse=self.lse, status=self.status)
-        B.spec_verify_greedy(logits, draft_tokens, kv_lens_in, self.k, workspace=self.greedy_ws,
-                             argmax_ids=self.argmax, accepted=self.accepted,
-                             next_tokens=self.next_tokens, kv_lens_out=self.kv_lens_out)
+        main.wait_stream(self.side)
         return self.out, self.lse, self.argmax, self.accepted, self.next_tokens, self.kv_lens_out
 
     @property
