@@ -7,7 +7,8 @@
 // next token a_n; kv_lens_out = kv_lens_in - (k - n).
 //
 // One launch.  The [T][V] fp32 logits are cut into chunks of C floats; each
-// CTA streams one chunk with coalesced 128-bit loads, reduces it to a 64-bit
+// CTA streams one chunk with coalesced 128-bit loads (eight in flight per
+// thread), reduces it to a 64-bit
 // key (order-preserving value bits << 32 | ~index, so the max key is the max
 // value at the lowest index) with warp shuffles, and parks the key in the
 // workspace.  The CTA that takes the last ticket reduces the keys per row,
@@ -31,6 +32,15 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) 
   if (u == 0x80000000u) u = 0u;  // -0 and +0 compare equal
   u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+
+// Streaming 16-byte load: bypass L1, ask L2 to fetch 256-byte sectors.
+__device__ __forceinline__ float4 ld_stream_f4(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
 }
 
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k) {
@@ -67,12 +77,13 @@ __global__ void __launch_bounds__(kGreedyThreads)
     const float4* p4 = reinterpret_cast<const float4*>(row + lo);
     const int n4 = (int)((hi - lo) >> 2);
     int i = tid;
-    for (; i + 3 * kGreedyThreads < n4; i += 4 * kGreedyThreads) {
-      float4 a[4];
+    // eight independent 16-byte loads per thread in flight per round
+    for (; i + 7 * kGreedyThreads < n4; i += 8 * kGreedyThreads) {
+      float4 a[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] = __ldcs(p4 + i + u * kGreedyThreads);
+      for (int u = 0; u < 8; ++u) a[u] = ld_stream_f4(p4 + i + u * kGreedyThreads);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const uint32_t base = (uint32_t)(lo + 4ll * (i + u * kGreedyThreads));
         if (best_i == 0xFFFFFFFFu) { best_v = a[u].x; best_i = base; }
         else if (a[u].x > best_v) { best_v = a[u].x; best_i = base; }
@@ -82,7 +93,7 @@ __global__ void __launch_bounds__(kGreedyThreads)
       }
     }
     for (; i < n4; i += kGreedyThreads) {
-      const float4 a = __ldcs(p4 + i);
+      const float4 a = ld_stream_f4(p4 + i);
       const uint32_t base = (uint32_t)(lo + 4ll * i);
       if (best_i == 0xFFFFFFFFu) { best_v = a.x; best_i = base; }
       else if (a.x > best_v) { best_v = a.x; best_i = base; }
@@ -142,10 +153,10 @@ __global__ void __launch_bounds__(kGreedyThreads)
 // workspace query and the launch agree.
 int greedy_chunk(int T, int V) {
   const long long total = (long long)T * V;
-  long long c = (total + 2 * 152 - 1) / (2 * 152);  // about two CTAs per SM
-  c = (c + 4095) / 4096 * 4096;
-  if (c < 4096) c = 4096;
-  if (c > 32768) c = 32768;
+  long long c = (total + 4 * 152 - 1) / (4 * 152);  // about four CTAs per SM
+  c = (c + 8191) / 8192 * 8192;
+  if (c < 8192) c = 8192;
+  if (c > 65536) c = 65536;
   return (int)c;
 }
 
