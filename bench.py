@@ -6,8 +6,10 @@ A step is one pass of the whole hot path on one synthetic batch: gated NoPE
 MLA verify attention (with its split-KV LSE merge) followed by the greedy
 verify (argmax, accepted prefix, trimmed kv_lens).  The default workload is
 the C=1 verify batch (1 request, k=7, 64 heads, context 1536, 163840-token
-vocabulary).  Inputs sit in HBM before timing; L2 (129 MB) is flushed by
-writing a 512 MB buffer before every timed step, outside the timed events.
+vocabulary).  Inputs sit in HBM before timing; L2 (129 MB) is flushed before
+every timed step, outside the timed events, by writing a 512 MB buffer and
+then reading a 256 MB one (so the flush's own dirty lines are written back
+before the step starts).
 
 --impl reference times the float64 CPU oracle on the same workload (host
 cores).  Under torchrun (N > 1) every rank runs an independent replica (the
@@ -35,7 +37,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="c1")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -115,7 +117,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -238,7 +240,16 @@ def main():
     logits = torch.from_numpy(inp["logits"]).to(device)
     drafts, kv_in = i32(inp["draft_tokens"]), i32(inp["kv_lens_in"])
     step = sv.VerifyStep(device, R, k, H, V, inp["max_pages"], num_splits=args.splits)
+    # L2 (129 MB) flush before every timed step: write 512 MB, then read
+    # 256 MB of another buffer so that the write-back of the dirty flush
+    # lines happens here and not inside the timed step
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+    flush_rd = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=device)
+    flush_sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def flush_l2():
+        flush.zero_()
+        torch.sum(flush_rd, dim=0, out=flush_sink)
 
     def run_step():
         return step(q, kv, bt, bounds, gate, inp["softmax_scale"], logits, drafts, kv_in)
@@ -253,7 +264,7 @@ def main():
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         for i in range(n):
-            flush.zero_()
+            flush_l2()
             starts[i].record()
             fn()
             ends[i].record()
@@ -356,7 +367,7 @@ def main():
         "data": "synthetic",
         "config": {"workload": f"{cfg.name}: {cfg.description}", "R": R, "k": k, "H": H, "T": T,
                    "vocab": V, "latent": 512, "page": 64, "num_splits": step.num_splits,
-                   "l2": "flushed (512 MB write) before every timed step, outside the events",
+                   "l2": "flushed before every timed step (512 MB write, then 256 MB read), outside the events",
                    "parallelism": f"replicas x{world}"},
         "attention_us": attn_mean * 1000.0,
         "attention_tflops": attn_tflops,

@@ -167,6 +167,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = rm / p.n_mtiles;
   const int Mq = p.H * p.q_per_req;
 
+  // warp 0: start the dependent loads of the set-up (bounds -> block table ->
+  // KV tiles) from L2 rather than HBM: prefetch the request's bound and
+  // block-table lines now
+  if (warp == 0) {
+    const int32_t* bt_row = p.block_table + (long long)r * p.max_pages;
+    for (int j = lane * 32; j < p.max_pages; j += 32 * 32) prefetch_l2(bt_row + j);
+    if (lane == 0) prefetch_l2(p.kv_bounds + r * p.q_per_req);
+    if (lane == 1) prefetch_l2(p.kv_bounds + r * p.q_per_req + p.q_per_req - 1);
+  }
   // softmax warps: start fetching this CTA's half of their query row now, so
   // the load overlaps the set-up below (row i of the tile <-> TMEM lane i)
   uint4 qv[32];
@@ -176,20 +185,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int u = 0; u < 32; ++u) qv[u] = (f0 < Mq) ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
   }
-
-  // ---- unit geometry (every thread derives the same values)
-  int maxb_req = 0;
-  for (int t = 0; t < p.q_per_req; ++t) maxb_req = max(maxb_req, load_bound(p, r * p.q_per_req + t));
-  const int t_first = (m_tile * kMTile) / p.H;
-  const int t_last = min((m_tile * kMTile + kMTile - 1) / p.H, p.q_per_req - 1);
-  int maxb_tile = 0;
-  for (int t = t_first; t <= t_last; ++t)
-    maxb_tile = max(maxb_tile, load_bound(p, r * p.q_per_req + t));
-  const int n_r = (maxb_req + kTileN - 1) / kTileN;
-  const int lo = (int)((long long)s_idx * n_r / S);
-  const int hi = (int)((long long)(s_idx + 1) * n_r / S);
-  const int hi_eff = min(hi, (maxb_tile + kTileN - 1) / kTileN);
-  const int ntiles = max(0, hi_eff - lo);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kOwnStages; ++s) {
@@ -219,6 +214,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // ---- unit geometry (every thread derives the same values)
+  int maxb_req = 0;
+  for (int t = 0; t < p.q_per_req; ++t) maxb_req = max(maxb_req, load_bound(p, r * p.q_per_req + t));
+  const int t_first = (m_tile * kMTile) / p.H;
+  const int t_last = min((m_tile * kMTile + kMTile - 1) / p.H, p.q_per_req - 1);
+  int maxb_tile = 0;
+  for (int t = t_first; t <= t_last; ++t)
+    maxb_tile = max(maxb_tile, load_bound(p, r * p.q_per_req + t));
+  const int n_r = (maxb_req + kTileN - 1) / kTileN;
+  const int lo = (int)((long long)s_idx * n_r / S);
+  const int hi = (int)((long long)(s_idx + 1) * n_r / S);
+  const int hi_eff = min(hi, (maxb_tile + kTileN - 1) / kTileN);
+  const int ntiles = max(0, hi_eff - lo);
+
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
