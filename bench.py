@@ -289,6 +289,15 @@ def main():
                                                     argmax_ids=step.argmax, accepted=step.accepted,
                                                     next_tokens=step.next_tokens,
                                                     kv_lens_out=step.kv_lens_out), args.steps)
+    # paged latent KV append of the k+1 verify rows (the step just before the
+    # attention); it rewrites the rows the pool already holds at those
+    # positions, so the attention inputs stay the same
+    pos_np = np.concatenate([np.arange(L - (k + 1), L) for L in inp["kv_lens_in"]]).astype(np.int32)
+    rows = [int(inp["block_table"][t // (k + 1)][p // 64]) * 64 + p % 64 for t, p in enumerate(pos_np)]
+    kv_new = kv.view(-1, 512)[torch.tensor(rows, dtype=torch.long, device=device)].contiguous()
+    positions = i32(pos_np)
+    append_ms = timed(lambda: sv.mla_kv_append(kv_new, positions, bt, kv, k + 1, status=step.status),
+                      args.steps)
     barrier()
     clocks = sampler.stop() if not args.no_clocks else None
 
@@ -327,6 +336,7 @@ def main():
         return m
 
     step_mean, attn_mean, greedy_mean, e2e_mean = (agg(step_ms), agg(attn_ms), agg(greedy_ms), agg(e2e_ms))
+    append_mean = agg(append_ms)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -374,12 +384,16 @@ def main():
         "greedy_us": greedy_mean * 1000.0,
         "greedy_gbps": greedy_gbps,
         "greedy_hbm_frac": greedy_gbps / peaks["hbm_gbs"],
+        "kv_append_us": append_mean * 1000.0,
+        "kv_append_gbps": T * 2 * 1024 / (append_mean * 1e-3) / 1e9,
         "steps_per_s_all_gpus": world * 1000.0 / step_mean,
         "roofline": roof,
         "cpu_baseline": base,
         "e2e": {"value": e2e_mean * 1000.0, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * step.launches_per_step,
+        "gpu_launches_all_timed_loops": args.steps * (2 * step.launches_per_step + 1 + 1
+                                                       + (1 if step.num_splits > 1 else 0) + 1),
         "clocks": clocks,
         "status_word": int(step.status.item()),
     }

@@ -11,6 +11,7 @@
  *                       latent rows, bounded per token, split over KV, with
  *                       the LSE merge and the sigmoid gate fused in.
  *   mla_lse_combine     the LSE merge + gate of split partials on its own.
+ *   mla_kv_append       the verify tokens' latent rows into the paged cache.
  *   spec_verify_greedy  target argmax, accepted draft prefix, next token and
  *                       trimmed per-request KV length.
  *
@@ -128,6 +129,33 @@ sv_status mla_verify_decode(const void* q_latent, const void* kv_pages, int num_
                             int H, float softmax_scale, int num_splits, void* workspace,
                             size_t workspace_bytes, void* out, float* lse, int32_t* status,
                             sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * mla_kv_append
+ *
+ * Writes the latent KV rows of the verify tokens into the paged cache before
+ * the attention reads them: the NoPE counterpart of the per-token KV write
+ * slot of "TensorRT-LLM PR #18166: Kimi K3 DSpark speculative decoding under
+ * Helix CP" (first commit message: global position -> write slot, -1 = not
+ * owned; on one GPU every position is owned).
+ *
+ * Token t (request r = t / q_per_req) with positions[t] = pos >= 0 stores
+ * kv_new[t] in page block_table[r][pos / 64], slot pos % 64; pos = -1 skips
+ * the token.  Positions of one call must be distinct per request.
+ *
+ *   kv_new       bf16 [T][512], 16-byte aligned (T = R*q_per_req).
+ *   positions    int32 [T].
+ *   block_table  int32 [R][max_pages_per_req].
+ *   kv_pages     bf16 [num_pages][page_size][512], 16-byte aligned, updated
+ *                in place.
+ *   page_size    must be 64.
+ *   status       device int32, ORed with SV_DEV_BAD_BOUND (pos past the
+ *                table) or SV_DEV_BAD_PAGE (entry outside the pool); such a
+ *                token is skipped.  May be NULL.
+ * ---------------------------------------------------------------------- */
+sv_status mla_kv_append(const void* kv_new, const int32_t* positions, const int32_t* block_table,
+                        int R, int q_per_req, int max_pages_per_req, void* kv_pages,
+                        int num_pages, int page_size, int32_t* status, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * mla_lse_combine

@@ -4,6 +4,7 @@ from .verify_ref import (  # noqa: F401
     gather_latent_rows,
     ref_attention_partials,
     ref_greedy_verify,
+    ref_kv_append,
     ref_lse_combine,
     ref_verify_attention,
     ref_verify_step,

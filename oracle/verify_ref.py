@@ -30,6 +30,12 @@ What it computes, written as the plain definitions (no blocking, no fusion):
   -inf set gives (-inf, 0) rather than NaN (the CP-merge weighting of
   "TensorRT-LLM PR #18166", second and third commits: corr = 0 for a
   zero-bound row, never 0 * NaN).
+* Paged KV append (``ref_kv_append``): the latent rows of the k+1 verify
+  tokens are written into the page pool at their positions before the
+  attention reads them: position pos of request r lands in page
+  block_table[r][pos // page_size], slot pos % page_size; a position of -1
+  writes nothing (the per-token KV write slot of "TensorRT-LLM PR #18166",
+  first commit message, "-1 = not owned"; one GPU owns every position).
 * Greedy verify (``ref_greedy_verify``): a_t = argmax_v logits[t, v] (lowest
   index on ties); accepted n_r = largest m <= k with d_j = a_{j-1} for all
   j <= m; next token a_{n_r}; the KV trims the rejected tail:
@@ -181,6 +187,23 @@ def ref_greedy_verify(logits, draft_tokens, kv_lens_in, k):
         nxt[r] = a[base + n]
         kv_out[r] = int(kv_lens_in[r]) - (k - n)
     return a, accepted, nxt, kv_out
+
+
+def ref_kv_append(kv_pages, block_table, positions, kv_new, q_per_req):
+    """Return a copy of the page pool with token t's latent row kv_new[t]
+    stored at its position (request r = t // q_per_req); -1 skips the token."""
+    pool = np.array(kv_pages, copy=True)
+    page_size = pool.shape[1]
+    for t, pos in enumerate(np.asarray(positions)):
+        pos = int(pos)
+        if pos < 0:
+            continue
+        r = t // q_per_req
+        page = int(block_table[r][pos // page_size])
+        if page < 0 or page >= pool.shape[0]:
+            raise ValueError("block table entry outside the page pool")
+        pool[page, pos % page_size] = kv_new[t]
+    return pool
 
 
 def ref_verify_step(inp: dict) -> dict:

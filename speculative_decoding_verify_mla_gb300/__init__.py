@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     greedy_workspace,
     greedy_workspace_bytes,
     load_library,
+    mla_kv_append,
     mla_lse_combine,
     mla_verify_decode,
     num_splits_for,

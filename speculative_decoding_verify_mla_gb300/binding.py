@@ -36,6 +36,7 @@ EXPORTED_SYMBOLS = (
     "mla_lse_combine",
     "sv_greedy_workspace_bytes",
     "spec_verify_greedy",
+    "mla_kv_append",
 )
 
 _lib = None
@@ -80,6 +81,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
             _c_void_p, _c_void_p, _c_void_p, _c_size, _c_void_p]
         lib.spec_verify_greedy.restype = _c_int
+        lib.mla_kv_append.argtypes = [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
+                                      _c_void_p, _c_int, _c_int, _c_void_p, _c_void_p]
+        lib.mla_kv_append.restype = _c_int
         _lib = lib
         return lib
 
@@ -227,3 +231,24 @@ def spec_verify_greedy(logits: torch.Tensor, draft_tokens: torch.Tensor, kv_lens
         _stream(dev))
     _check_status("spec_verify_greedy", code)
     return tuple(outs)
+
+
+def mla_kv_append(kv_new: torch.Tensor, positions: torch.Tensor, block_table: torch.Tensor,
+                  kv_pages: torch.Tensor, q_per_req: int, status: torch.Tensor | None = None):
+    """Write kv_new [T, 512] bf16 into kv_pages [P, 64, 512] (in place) at the
+    tokens' positions [T] int32 (-1 = skip) through block_table [R, max_pages]."""
+    lib = load_library()
+    _check(kv_new.dim() == 2 and kv_new.shape[1] == SV_LATENT_DIM, "kv_new must be [T, 512]")
+    T = kv_new.shape[0]
+    R, max_pages = block_table.shape
+    _check(T == R * q_per_req, "T must equal R * q_per_req")
+    dev = kv_new.device
+    for name, t, dt in (("kv_new", kv_new, torch.bfloat16), ("kv_pages", kv_pages, torch.bfloat16),
+                        ("positions", positions, torch.int32), ("block_table", block_table, torch.int32)):
+        _check(t.dtype == dt and t.device == dev and t.is_contiguous(), f"{name}: {dt}, contiguous, on {dev}")
+    _check(tuple(positions.shape) == (T,), "positions must be [T]")
+    code = lib.mla_kv_append(_ptr(kv_new), _ptr(positions), _ptr(block_table), R, q_per_req,
+                             max_pages, _ptr(kv_pages), int(kv_pages.shape[0]),
+                             int(kv_pages.shape[1]), _ptr(status), _stream(dev))
+    _check_status("mla_kv_append", code)
+    return kv_pages

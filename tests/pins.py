@@ -334,3 +334,52 @@ def check_bf16_rounding():
     for v, bits in bf16_round_cases():
         got = int(f32_to_bf16_bits(np.array([v], dtype=np.float32))[0])
         assert got == bits, (v, hex(got), hex(bits))
+
+
+# --------------------------------------------------------------------------
+# KV append pins: the definition is a scatter, so the pins are properties that
+# do not restate it: read-back through the independent page walk, untouched
+# rows, skipped tokens, and page-order invariance.
+# --------------------------------------------------------------------------
+def pin_kv_append(orc):
+    cfg = small_config("c0", R=3, k=2, H=2, kv_lens=(5, 130, 64), shuffled=True, vocab=64)
+    inp = make_inputs(cfg, seed=9)
+    k1 = inp["k"] + 1
+    rng = np.random.default_rng(9)
+    T = inp["T"]
+    kv_new = f32_to_bf16_bits(rng.standard_normal((T, inp["D"]), dtype=np.float32))
+    # verify-group positions L-k-1 .. L-1; the middle token of request 1 is skipped
+    pos = np.concatenate([np.arange(L - k1, L) for L in inp["kv_lens_in"]]).astype(np.int32)
+    pos[k1 + 1] = -1
+    pool = orc.ref_kv_append(inp["kv_bits"], inp["block_table"], pos, kv_new, k1)
+    # read back through an inverse page walk (independent of the scatter)
+    owner = {}
+    for r in range(inp["R"]):
+        for i, p in enumerate(inp["block_table"][r]):
+            if p >= 0:
+                owner[int(p)] = (r, i)
+    written = set()
+    for t in range(T):
+        if pos[t] < 0:
+            continue
+        r = t // k1
+        hits = [(p, s) for p, (rr, i) in owner.items() if rr == r for s in range(64) if i * 64 + s == pos[t]]
+        assert len(hits) == 1
+        p, s = hits[0]
+        assert np.array_equal(pool[p, s], kv_new[t])
+        written.add((p, s))
+    # everything else is untouched, including the skipped token's slot
+    for p in range(pool.shape[0]):
+        for s in range(64):
+            if (p, s) not in written:
+                assert np.array_equal(pool[p, s], inp["kv_bits"][p, s])
+    assert len(written) == T - 1
+    # relabelling the pages commutes with the append
+    perm = np.random.default_rng(2).permutation(pool.shape[0])
+    kv2 = np.empty_like(inp["kv_bits"]); kv2[perm] = inp["kv_bits"]
+    bt2 = np.where(inp["block_table"] >= 0, perm[np.maximum(inp["block_table"], 0)], -1)
+    pool2 = orc.ref_kv_append(kv2, bt2, pos, kv_new, k1)
+    assert np.array_equal(pool2[perm], pool)
+
+
+ALL_PINS.append(pin_kv_append)

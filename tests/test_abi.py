@@ -102,3 +102,12 @@ def test_greedy_host_checks(lib):
     assert f(4096, 8, 10, 2, 3, None, 4096, 4096, 4096, 4096, 4096, 4096, 1 << 20, None) == 1  # drafts
     assert f(4096, 8, 10, 2, 3, 4096, 4096, 4096, 4096, 4096, 4096, 4096, 8, None) == 4      # workspace
     assert f(4096, 8, 10, 2, 3, 4096, 4096, 4096, 4096, 4096, 4096, 4096 + 16, 1 << 20, None) == 3
+
+
+def test_kv_append_host_checks(lib):
+    f = lib.mla_kv_append
+    assert f(4096, 4096, 4096, 2, 4, 2, 4096, 4, 32, None, None) == 5   # page size
+    assert f(4096, 4096, 4096, -1, 4, 2, 4096, 4, 64, None, None) == 2
+    assert f(4096, 4096, 4096, 0, 4, 2, 4096, 4, 64, None, None) == 0   # nothing to do
+    assert f(None, 4096, 4096, 2, 4, 2, 4096, 4, 64, None, None) == 1
+    assert f(4096 + 8, 4096, 4096, 2, 4, 2, 4096, 4, 64, None, None) == 3

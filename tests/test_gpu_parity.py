@@ -314,3 +314,63 @@ def test_verify_step_object(sv):
     check_attention(res[0], res[1], ref["out"], ref["lse"], label="step")
     for g, key in zip(res[2:], ("argmax", "accepted", "next_tokens", "kv_lens_out")):
         assert np.array_equal(g.cpu().numpy(), ref[key])
+
+
+# ----------------------------------------------------------------- KV append
+def _append_case(seed=10):
+    cfg = small_config("c2", R=5, k=4, H=8, kv_lens=(64, 65, 700, 130, 5), kv_len_range=None,
+                       shuffled=True, vocab=64)
+    inp = make_inputs(cfg, seed=seed)
+    k1 = inp["k"] + 1
+    rng = np.random.default_rng(seed)
+    from workloads import f32_to_bf16_bits
+    kv_new = f32_to_bf16_bits(rng.standard_normal((inp["T"], 512), dtype=np.float32))
+    pos = np.concatenate([np.arange(L - k1, L) for L in inp["kv_lens_in"]]).astype(np.int32)
+    pos[3] = -1  # one token not written
+    return inp, kv_new, pos
+
+
+def test_kv_append_bit_exact(sv):
+    inp, kv_new, pos = _append_case()
+    k1 = inp["k"] + 1
+    ref_pool = oracle.ref_kv_append(inp["kv_bits"], inp["block_table"], pos, kv_new, k1)
+    d = device_inputs(inp, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sv.mla_kv_append(bf16_tensor(kv_new, DEV), i32(pos, DEV), d["block_table"], d["kv"], k1, status=status)
+    torch.cuda.synchronize()
+    got = d["kv"].view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, ref_pool)
+    assert int(status.item()) == 0
+
+
+def test_kv_append_then_attention(sv):
+    """Append the verify rows, then attend: equals the oracle on the appended pool."""
+    inp, kv_new, pos = _append_case(seed=11)
+    k1 = inp["k"] + 1
+    pool = oracle.ref_kv_append(inp["kv_bits"], inp["block_table"], pos, kv_new, k1)
+    ref_o, ref_l = oracle.ref_verify_attention(inp["q_bits"], pool, inp["block_table"], inp["kv_bounds"],
+                                               inp["gate_bits"], k1, inp["softmax_scale"])
+    d = device_inputs(inp, DEV)
+    sv.mla_kv_append(bf16_tensor(kv_new, DEV), i32(pos, DEV), d["block_table"], d["kv"], k1)
+    out, lse = sv.mla_verify_decode(d["q"], d["kv"], d["block_table"], d["kv_bounds"], d["gate"], k1,
+                                    inp["softmax_scale"])
+    torch.cuda.synchronize()
+    check_attention(out, lse, ref_o, ref_l, label="append+attention")
+
+
+def test_kv_append_bad_data(sv):
+    inp, kv_new, pos = _append_case(seed=12)
+    k1 = inp["k"] + 1
+    d = device_inputs(inp, DEV)
+    before = d["kv"].clone()
+    bad = pos.copy()
+    bad[0] = inp["max_pages"] * 64 + 5  # past the block table
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sv.mla_kv_append(bf16_tensor(kv_new, DEV), i32(bad, DEV), d["block_table"], d["kv"], k1, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & sv.SV_DEV_BAD_BOUND
+    # the bad token wrote nothing; the others match the oracle
+    bad[0] = -1
+    ref_pool = oracle.ref_kv_append(before.view(torch.int16).cpu().numpy().view(np.uint16),
+                                    inp["block_table"], bad, kv_new, k1)
+    assert np.array_equal(d["kv"].view(torch.int16).cpu().numpy().view(np.uint16), ref_pool)
