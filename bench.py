@@ -78,10 +78,15 @@ def workload_figures(inp):
     return attn_flops, attn_bytes, logits_bytes
 
 
+# the sources that compile into the attention kernel whose DRAM traffic the
+# committed ncu summary records
+ATTENTION_SOURCES = ("mla_verify_decode.cu", "sv_ptx.cuh")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verify_mla_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in ATTENTION_SOURCES:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
