@@ -10,3 +10,4 @@ from .verify_ref import (  # noqa: F401
     ref_verify_step,
     sigmoid,
 )
+from .sampled_ref import inverse_cdf, ref_sampled_verify, target_probs  # noqa: F401

@@ -383,3 +383,119 @@ def pin_kv_append(orc):
 
 
 ALL_PINS.append(pin_kv_append)
+
+
+# --------------------------------------------------------------------------
+# sampled (rejection-sampling) verification
+# --------------------------------------------------------------------------
+# Pins independent of the oracle's formulas: the defining property of
+# speculative sampling (every emitted token is distributed as the target
+# distribution, whatever the draft distribution), checked by Monte Carlo with a
+# chi-square test; hand-derived accept/reject and draw cases; scipy's softmax;
+# the closed form q = p (every draft accepted); and the low-temperature limit,
+# where sampled verification with one-hot drafts must equal greedy
+# verification.
+def _mc_emitted(orc, p_rows, q_rows, trials, seed):
+    """Run the oracle on `trials` independent draws of (drafts ~ q, uniforms)
+    and return the emitted tokens per position (-1 where not emitted)."""
+    rng = np.random.default_rng(seed)
+    k = q_rows.shape[0]
+    V = p_rows.shape[1]
+    logits = np.log(p_rows).astype(np.float64)
+    R = trials
+    drafts = np.stack([rng.choice(V, size=R, p=q_rows[j]) for j in range(k)], axis=1)
+    uni = rng.random((R, k + 1))
+    a, nxt, _ = orc.ref_sampled_verify(np.tile(logits, (R, 1)), drafts, np.tile(q_rows, (R, 1, 1)),
+                                       uni, np.full(R, 100), k, 1.0)
+    emitted = np.full((R, k + 1), -1, dtype=np.int64)
+    for r in range(R):
+        n = int(a[r])
+        emitted[r, :n] = drafts[r, :n]
+        emitted[r, n] = nxt[r]
+    return emitted
+
+
+def _chi2_ok(samples, p, alpha=1e-6):
+    from scipy.stats import chisquare
+    counts = np.bincount(samples, minlength=len(p)).astype(np.float64)
+    expected = p * counts.sum()
+    keep = expected > 0
+    assert counts[~keep].sum() == 0, "a token of zero target probability was emitted"
+    return chisquare(counts[keep], expected[keep]).pvalue > alpha
+
+
+def pin_sampled_distribution(orc):
+    """Each emitted position is distributed as the target row it verifies."""
+    p = np.array([[0.40, 0.25, 0.15, 0.10, 0.06, 0.04],
+                  [0.05, 0.05, 0.50, 0.10, 0.20, 0.10],
+                  [0.30, 0.30, 0.10, 0.10, 0.10, 0.10]])
+    q = np.array([[0.05, 0.50, 0.05, 0.30, 0.05, 0.05],
+                  [0.30, 0.10, 0.10, 0.10, 0.30, 0.10]])
+    em = _mc_emitted(orc, p, q, trials=6000, seed=123)
+    assert _chi2_ok(em[:, 0], p[0]), "first emitted token is not distributed as p_0"
+    sel = em[:, 1] >= 0
+    assert sel.sum() > 1000 and _chi2_ok(em[sel, 1], p[1]), "second emitted token is not p_1"
+    sel = em[:, 2] >= 0
+    assert sel.sum() > 300 and _chi2_ok(em[sel, 2], p[2]), "bonus token is not p_2"
+
+
+def pin_sampled_hand_cases(orc):
+    p = np.array([0.5, 0.3, 0.2])
+    q = np.array([[0.2, 0.7, 0.1]])
+    x = np.log(p)[None, :].repeat(2, axis=0)
+
+    def run(u0, u1):
+        a, nxt, kv = orc.ref_sampled_verify(x, [[1]], q[None], np.array([[u0, u1]]), [50], 1, 1.0)
+        return int(a[0]), int(nxt[0]), int(kv[0])
+    # accept iff u * 0.7 < 0.3, i.e. u < 3/7 = 0.42857...
+    assert run(0.42, 0.5)[0] == 1
+    assert run(0.43, 0.5)[0] == 0
+    # rejected: residual max(0, p - q) = [0.3, 0, 0.1], total 0.4
+    assert run(0.43, 0.74) == (0, 0, 49)   # 0.74 * 0.4 = 0.296 < 0.3
+    assert run(0.43, 0.76) == (0, 2, 49)   # 0.304 > 0.3: skips the zero-weight id 1
+    # accepted: the bonus token is drawn from p of the last verify token
+    assert run(0.1, 0.49) == (1, 0, 50)
+    assert run(0.1, 0.51) == (1, 1, 50)
+    assert run(0.1, 0.81) == (1, 2, 50)
+    # inverse CDF on its own
+    assert orc.inverse_cdf(np.array([1.0, 0.0, 3.0]), 0.2) == 0
+    assert orc.inverse_cdf(np.array([1.0, 0.0, 3.0]), 0.25) == 2
+    assert orc.inverse_cdf(np.array([0.0, 0.0, 5.0]), 0.0) == 2
+    assert orc.inverse_cdf(np.array([2.0, 2.0]), 0.0) == 0
+
+
+def pin_sampled_closed_forms(orc):
+    from scipy.special import softmax
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 40)) * 2
+    for temp in (0.5, 1.0, 3.0):
+        assert np.allclose(orc.target_probs(x[0], temp), softmax(x[0] / temp), rtol=1e-12, atol=0)
+    # q = p at every position: every draft is accepted, whatever u < 1
+    k, R = 2, 50
+    temp = 0.7
+    xs = rng.standard_normal((R * (k + 1), 40))
+    qp = np.stack([np.stack([softmax(xs[r * (k + 1) + j] / temp) for j in range(k)]) for r in range(R)])
+    drafts = rng.integers(0, 40, size=(R, k))
+    uni = rng.random((R, k + 1)) * 0.999999
+    a, nxt, kv = orc.ref_sampled_verify(xs, drafts, qp, uni, np.full(R, 10), k, temp)
+    assert np.all(a == k) and np.all(kv == 10)
+
+
+def pin_sampled_greedy_limit(orc):
+    """Low temperature + one-hot drafts = greedy verification."""
+    inp = make_inputs(small_config("c0", vocab=512), seed=4)
+    R, k = inp["R"], inp["k"]
+    V = inp["logits"].shape[1]
+    a_g, n_g, nxt_g, kv_g = orc.ref_greedy_verify(inp["logits"], inp["draft_tokens"], inp["kv_lens_in"], k)
+    onehot = np.zeros((R, k, V))
+    for r in range(R):
+        for j in range(k):
+            onehot[r, j, inp["draft_tokens"][r][j]] = 1.0
+    uni = np.random.default_rng(1).random((R, k + 1)) * 0.98 + 0.01
+    a, nxt, kv = orc.ref_sampled_verify(inp["logits"], inp["draft_tokens"], onehot, uni, inp["kv_lens_in"],
+                                        k, 1e-3)
+    assert np.array_equal(a, n_g) and np.array_equal(nxt, nxt_g) and np.array_equal(kv, kv_g)
+
+
+SAMPLED_PINS = [pin_sampled_distribution, pin_sampled_hand_cases, pin_sampled_closed_forms,
+                pin_sampled_greedy_limit]

@@ -11,6 +11,11 @@ def test_pin(pin):
     pin(oracle)
 
 
+@pytest.mark.parametrize("pin", pins.SAMPLED_PINS, ids=lambda f: f.__name__)
+def test_sampled_pin(pin):
+    pin(oracle)
+
+
 def test_bf16_rounding():
     pins.check_bf16_rounding()
 

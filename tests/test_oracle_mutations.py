@@ -150,3 +150,46 @@ def test_some_pin_catches(mutate):
         except (AssertionError, ValueError, IndexError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught {mutate.__name__}"
+
+
+# --------------------------------------------------------------------------
+# sampled verification: each mutation rewrites one expression of a private
+# copy of the sampled-verification oracle's source
+# --------------------------------------------------------------------------
+SAMPLED_MUTATIONS = {
+    "residual_not_clipped": ("w = np.maximum(p - qd[r, j], 0.0)", "w = p - qd[r, j]"),
+    "residual_is_target": ("w = np.maximum(p - qd[r, j], 0.0)", "w = p.copy()"),
+    "ratio_inverted": ("lhs, rhs = u[r, j] * qd[r, j, d], p[d]", "lhs, rhs = u[r, j] * p[d], qd[r, j, d]"),
+    "bonus_wrong_row": ("w = target_probs(x[base + k], temperature)",
+                        "w = target_probs(x[base + k - 1], temperature)"),
+    "cdf_left_side": ('side="right"', 'side="left"'),
+    "temperature_multiplies": ("/ float(temperature)", "* float(temperature)"),
+    "trim_wrong": ("int(kv_lens_in[r]) - (k - n)", "int(kv_lens_in[r]) - n"),
+    "accepted_counts_rejected": ("            n = j\n", "            n = j + 1\n"),
+}
+
+
+def _sampled_mutant(old, new):
+    import types
+    spec = importlib.util.find_spec("oracle.sampled_ref")
+    src = open(spec.origin).read()
+    assert src.count(old) >= 1, old
+    mod = types.ModuleType("_sampled_mutant")
+    exec(compile(src.replace(old, new), spec.origin, "exec"), mod.__dict__)
+    # the greedy oracle is needed by the greedy-limit pin
+    import oracle
+    mod.ref_greedy_verify = oracle.ref_greedy_verify
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(SAMPLED_MUTATIONS))
+def test_some_sampled_pin_catches(name):
+    m = _sampled_mutant(*SAMPLED_MUTATIONS[name])
+    caught = []
+    for pin in pins.SAMPLED_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(m)
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught {name}"

@@ -209,6 +209,49 @@ def make_inputs(cfg: VerifyConfig | str, seed: int = 0) -> dict:
     )
 
 
+def make_sampled_inputs(cfg: VerifyConfig | str, seed: int = 0, temperature: float = 1.0,
+                        draft_mix: tuple[float, float] = (0.05, 0.95)) -> dict:
+    """Inputs of sampled verification for one batch (numpy, host memory).
+
+    Its own random stream (seed, 2), so it does not disturb ``make_inputs``.
+    Target logits follow the same recipe as ``make_inputs`` (N(0, sd) clipped
+    to +-5.5 sd, one planted id per row at 6 sd).  Draft position j of request
+    r has the distribution q = (1 - a_r) * onehot(planted id of token j) +
+    a_r * E / sum(E), E ~ Exp(1) iid over the vocabulary, a_r ~ U(draft_mix),
+    stored as float32; the draft token is drawn from q (numpy's categorical
+    draw).  Uniforms [R][k+1] ~ U[0, 1)."""
+    if isinstance(cfg, str):
+        cfg = CONFIGS[cfg]
+    rng = np.random.default_rng([seed, 2])
+    R, k, V, sd = cfg.R, cfg.k, cfg.vocab, cfg.logit_sd
+    T = R * (k + 1)
+    if cfg.kv_lens is not None:
+        kv_lens = np.asarray(cfg.kv_lens, dtype=np.int32)
+    else:
+        lo, hi = cfg.kv_len_range
+        kv_lens = rng.integers(lo, hi + 1, size=R).astype(np.int32)
+    logits = np.empty((T, V), dtype=np.float32)
+    for t in range(T):
+        logits[t] = np.clip(rng.standard_normal(V, dtype=np.float32) * np.float32(sd),
+                            -5.5 * sd, 5.5 * sd)
+    planted = rng.integers(0, V, size=T).astype(np.int32)
+    logits[np.arange(T), planted] = np.float32(6.0 * sd)
+    mix = rng.uniform(draft_mix[0], draft_mix[1], size=R)
+    draft_probs = np.empty((R, k, V), dtype=np.float32)
+    drafts = np.empty((R, k), dtype=np.int32)
+    for r in range(R):
+        for j in range(k):
+            e = rng.exponential(1.0, size=V)
+            q = mix[r] * e / e.sum()
+            q[planted[r * (k + 1) + j]] += 1.0 - mix[r]
+            draft_probs[r, j] = q.astype(np.float32)
+            drafts[r, j] = rng.choice(V, p=q / q.sum())
+    uniforms = rng.random((R, k + 1)).astype(np.float32)
+    return dict(cfg=cfg, seed=seed, R=R, k=k, T=T, V=V, temperature=float(temperature),
+                kv_lens_in=kv_lens, logits=logits, planted_argmax=planted,
+                draft_probs=draft_probs, draft_tokens=drafts, uniforms=uniforms)
+
+
 def small_config(base: str | VerifyConfig = "c0", **overrides) -> VerifyConfig:
     """A variant of a named configuration (edge cases, test sweeps)."""
     if isinstance(base, str):
