@@ -303,6 +303,20 @@ def main():
     positions = i32(pos_np)
     append_ms = timed(lambda: sv.mla_kv_append(kv_new, positions, bt, kv, k + 1, status=step.status),
                       args.steps)
+    # sampled (rejection-sampling) verification on the same logits shape, with
+    # seeded draft distributions and uniforms
+    from workloads import make_sampled_inputs
+    sinp = make_sampled_inputs(cfg, seed=rank)
+    s_logits = torch.from_numpy(sinp["logits"]).to(device)
+    s_drafts, s_kv = i32(sinp["draft_tokens"]), i32(sinp["kv_lens_in"])
+    s_probs = torch.from_numpy(sinp["draft_probs"]).to(device)
+    s_uni = torch.from_numpy(sinp["uniforms"]).to(device)
+    s_ws = sv.sampled_workspace(device, R, k, V)
+    s_out = [torch.empty(R, dtype=torch.int32, device=device) for _ in range(3)]
+    sampled_ms = timed(lambda: sv.spec_verify_sampled(s_logits, s_drafts, s_probs, s_uni, s_kv, k,
+                                                      temperature=sinp["temperature"], workspace=s_ws,
+                                                      accepted=s_out[0], next_tokens=s_out[1],
+                                                      kv_lens_out=s_out[2]), args.steps)
     barrier()
     clocks = sampler.stop() if not args.no_clocks else None
 
@@ -342,6 +356,7 @@ def main():
 
     step_mean, attn_mean, greedy_mean, e2e_mean = (agg(step_ms), agg(attn_ms), agg(greedy_ms), agg(e2e_ms))
     append_mean = agg(append_ms)
+    sampled_mean = agg(sampled_ms)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -391,6 +406,8 @@ def main():
         "greedy_hbm_frac": greedy_gbps / peaks["hbm_gbs"],
         "kv_append_us": append_mean * 1000.0,
         "kv_append_gbps": T * 2 * 1024 / (append_mean * 1e-3) / 1e9,
+        "sampled_verify_us": sampled_mean * 1000.0,
+        "sampled_verify_gbps": (T + 2 * R) * V * 4 / (sampled_mean * 1e-3) / 1e9,
         "steps_per_s_all_gpus": world * 1000.0 / step_mean,
         "roofline": roof,
         "cpu_baseline": base,
@@ -398,7 +415,7 @@ def main():
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * step.launches_per_step,
         "gpu_launches_all_timed_loops": args.steps * (2 * step.launches_per_step + 1 + 1
-                                                       + (1 if step.num_splits > 1 else 0) + 1),
+                                                       + (1 if step.num_splits > 1 else 0) + 1 + 2),
         "clocks": clocks,
         "status_word": int(step.status.item()),
     }

@@ -12,6 +12,7 @@
  *                       the LSE merge and the sigmoid gate fused in.
  *   mla_lse_combine     the LSE merge + gate of split partials on its own.
  *   mla_kv_append       the verify tokens' latent rows into the paged cache.
+ *   spec_verify_sampled rejection-sampling verification (probabilistic drafts).
  *   spec_verify_greedy  target argmax, accepted draft prefix, next token and
  *                       trimmed per-request KV length.
  *
@@ -208,6 +209,51 @@ sv_status spec_verify_greedy(const float* logits, int T, int V, int R, int k,
                              int32_t* argmax_ids, int32_t* accepted, int32_t* next_tokens,
                              int32_t* kv_lens_out, void* workspace, size_t workspace_bytes,
                              sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * spec_verify_sampled
+ *
+ * Sampled verification with KV trim ("M* PR #257", section "Speculative
+ * decoding": verification is greedy or sampled, FlashInfer's chain sampling;
+ * the model card "RedHatAI/Kimi-K3-speculator.dspark", section "Deployment",
+ * draws the drafts probabilistically).  The pages give no formula; this is
+ * token-wise chain rejection sampling (speculative sampling, Leviathan et al.
+ * 2023; Chen et al. 2023):
+ *     p_t        = softmax(logits[t] / temperature),  t = r*(k+1) + j
+ *     draft j    accepted iff uniforms[r][j] * q(d) < p_t(d),
+ *                d = draft_tokens[r][j], q = draft_probs[r][j]
+ *                (a draft id outside [0, V) is rejected)
+ *     accepted[r]   = n = number of drafts before the first rejection
+ *     next_tokens[r]= draw from max(0, p_t - q) at the first rejection
+ *                     (p_t if that is zero everywhere), or from p of token
+ *                     r*(k+1)+k when all k are accepted; a draw from weights
+ *                     w with u = uniforms[r][k] is the smallest v with
+ *                     sum_{i<=v} w_i > u * sum(w)
+ *     kv_lens_out[r]= kv_lens_in[r] - (k - n)
+ * Arithmetic is fp32 on the device: a decision whose margin is within fp32
+ * rounding (|u*q - p| ~ 1e-6 relative, or u*W within ~1e-5 W of a CDF step)
+ * may fall either way.
+ *
+ *   logits        fp32 [R*(k+1)][V], finite, V >= 1.
+ *   temperature   > 0 and finite; logits / temperature must stay finite.
+ *   draft_tokens  int32 [R][k];  draft_probs fp32 [R][k][V] (each row the
+ *                 distribution its draft was drawn from).  Both may be NULL
+ *                 when k == 0.
+ *   uniforms      fp32 [R][k+1] in [0, 1): the caller's random numbers.
+ *   kv_lens_in    int32 [R];  accepted, next_tokens, kv_lens_out int32 [R].
+ *   workspace     sv_sampled_workspace_bytes(R, k, V) bytes, 256-byte
+ *                 aligned, zero-filled before its first use; every call leaves
+ *                 its counters zero again.  Calls sharing one workspace must
+ *                 not run concurrently.
+ * Two kernels on `stream` (the second a programmatic dependent launch).
+ * ---------------------------------------------------------------------- */
+size_t sv_sampled_workspace_bytes(int R, int k, int V);
+
+sv_status spec_verify_sampled(const float* logits, int R, int k, int V, float temperature,
+                              const int32_t* draft_tokens, const float* draft_probs,
+                              const float* uniforms, const int32_t* kv_lens_in,
+                              int32_t* accepted, int32_t* next_tokens, int32_t* kv_lens_out,
+                              void* workspace, size_t workspace_bytes, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * spec_verify_greedy_noalloc

@@ -17,7 +17,10 @@ from .binding import (  # noqa: F401
     mla_lse_combine,
     mla_verify_decode,
     num_splits_for,
+    sampled_workspace,
+    sampled_workspace_bytes,
     spec_verify_greedy,
+    spec_verify_sampled,
     status_string,
 )
 from .step import VerifyStep  # noqa: F401

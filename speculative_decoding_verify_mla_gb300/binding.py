@@ -37,6 +37,8 @@ EXPORTED_SYMBOLS = (
     "sv_greedy_workspace_bytes",
     "spec_verify_greedy",
     "mla_kv_append",
+    "sv_sampled_workspace_bytes",
+    "spec_verify_sampled",
 )
 
 _lib = None
@@ -84,6 +86,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.mla_kv_append.argtypes = [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
                                       _c_void_p, _c_int, _c_int, _c_void_p, _c_void_p]
         lib.mla_kv_append.restype = _c_int
+        lib.sv_sampled_workspace_bytes.argtypes = [_c_int, _c_int, _c_int]
+        lib.sv_sampled_workspace_bytes.restype = _c_size
+        lib.spec_verify_sampled.argtypes = [
+            _c_void_p, _c_int, _c_int, _c_int, _c_float, _c_void_p, _c_void_p, _c_void_p,
+            _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_size, _c_void_p]
+        lib.spec_verify_sampled.restype = _c_int
         _lib = lib
         return lib
 
@@ -252,3 +260,59 @@ def mla_kv_append(kv_new: torch.Tensor, positions: torch.Tensor, block_table: to
                              int(kv_pages.shape[1]), _ptr(status), _stream(dev))
     _check_status("mla_kv_append", code)
     return kv_pages
+
+
+def sampled_workspace_bytes(R: int, k: int, V: int) -> int:
+    return int(load_library().sv_sampled_workspace_bytes(R, k, V))
+
+
+_sampled_ws: dict = {}
+
+
+def sampled_workspace(device, R: int, k: int, V: int) -> torch.Tensor:
+    """A zero-filled workspace for spec_verify_sampled, cached per device and
+    size (the kernels leave its counters zero after every call)."""
+    key = (str(device), sampled_workspace_bytes(R, k, V))
+    ws = _sampled_ws.get(key)
+    if ws is None:
+        ws = torch.zeros(key[1], dtype=torch.uint8, device=device)
+        _sampled_ws[key] = ws
+    return ws
+
+
+def spec_verify_sampled(logits: torch.Tensor, draft_tokens: torch.Tensor, draft_probs: torch.Tensor,
+                        uniforms: torch.Tensor, kv_lens_in: torch.Tensor, k: int,
+                        temperature: float = 1.0, workspace: torch.Tensor | None = None,
+                        accepted: torch.Tensor | None = None, next_tokens: torch.Tensor | None = None,
+                        kv_lens_out: torch.Tensor | None = None):
+    """Rejection-sampling verification.  logits [R*(k+1), V] fp32, draft_tokens
+    [R, k] int32, draft_probs [R, k, V] fp32, uniforms [R, k+1] fp32, kv_lens_in
+    [R] int32.  Returns (accepted, next_tokens, kv_lens_out), each [R] int32."""
+    lib = load_library()
+    _check(logits.dim() == 2, "logits must be [T, V]")
+    T, V = logits.shape
+    R = kv_lens_in.shape[0]
+    _check(T == R * (k + 1), "T must equal R * (k + 1)")
+    dev = logits.device
+    _check(dev.type == "cuda", "tensors must live on a CUDA device")
+    checks = [("logits", logits, torch.float32), ("uniforms", uniforms, torch.float32),
+              ("kv_lens_in", kv_lens_in, torch.int32)]
+    if k > 0:
+        checks += [("draft_tokens", draft_tokens, torch.int32), ("draft_probs", draft_probs, torch.float32)]
+        _check(tuple(draft_tokens.shape) == (R, k), "draft_tokens must be [R, k]")
+        _check(tuple(draft_probs.shape) == (R, k, V), "draft_probs must be [R, k, V]")
+    for name, t, dt in checks:
+        _check(t.dtype == dt and t.device == dev and t.is_contiguous(), f"{name}: {dt}, contiguous, on {dev}")
+    _check(tuple(uniforms.shape) == (R, k + 1), "uniforms must be [R, k+1]")
+    if workspace is None:
+        workspace = sampled_workspace(dev, R, k, V)
+    outs = []
+    for o in (accepted, next_tokens, kv_lens_out):
+        outs.append(torch.empty(R, dtype=torch.int32, device=dev) if o is None else o)
+    code = lib.spec_verify_sampled(
+        _ptr(logits), R, k, V, float(temperature), _ptr(draft_tokens) if k > 0 else None,
+        _ptr(draft_probs) if k > 0 else None, _ptr(uniforms), _ptr(kv_lens_in),
+        _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(dev))
+    _check_status("spec_verify_sampled", code)
+    return tuple(outs)

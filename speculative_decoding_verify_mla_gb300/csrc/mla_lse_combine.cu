@@ -46,8 +46,8 @@ __global__ void __launch_bounds__(kCombineThreads)
 
   // split weights: lane s holds lse_s for s = lane and lane + 32
   float l0 = -INFINITY, l1 = -INFINITY;
-  if (lane < S) l0 = __ldg(part_lse + (long long)lane * rows + row);
-  if (lane + 32 < S) l1 = __ldg(part_lse + (long long)(lane + 32) * rows + row);
+  if (lane < S) l0 = ld_dep_f32(part_lse + (long long)lane * rows + row);
+  if (lane + 32 < S) l1 = ld_dep_f32(part_lse + (long long)(lane + 32) * rows + row);
   float m = fmaxf(l0, l1);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kCombineThreads)
         const float* src = part_o + ((long long)min(s, S - 1) * rows + row) * 512 + col0;
 #pragma unroll
         for (int j = 0; j < 2; ++j)
-          v[u][j] = (ws[u] != 0.f) ? __ldcs(reinterpret_cast<const float4*>(src + 128 * j))
+          v[u][j] = (ws[u] != 0.f) ? ld_dep_f4_stream(reinterpret_cast<const float4*>(src + 128 * j))
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll

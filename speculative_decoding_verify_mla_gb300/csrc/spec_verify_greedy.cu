@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kGreedyThreads = 256;
 constexpr size_t kGreedyHeader = 256;  // ticket counter, padded
+constexpr int kTailRows = 1024;        // rows / requests the shared-memory tail handles
 
 __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
   uint32_t u = __float_as_uint(v);
@@ -61,6 +62,9 @@ __global__ void __launch_bounds__(kGreedyThreads)
                          int32_t* __restrict__ kv_lens_out, unsigned int* __restrict__ ticket,
                          unsigned long long* __restrict__ keys) {
   __shared__ unsigned long long s_warp[kGreedyThreads / 32];
+  __shared__ unsigned long long s_key[kTailRows];
+  __shared__ int s_arg[kTailRows];
+  __shared__ int s_n[kTailRows];
   __shared__ bool s_last;
   const int tid = threadIdx.x;
   const long long bid = blockIdx.x;
@@ -124,27 +128,59 @@ __global__ void __launch_bounds__(kGreedyThreads)
   __syncthreads();
   if (!s_last) return;
 
-  // ---- last CTA: per-row argmax (one warp per row), then acceptance and trim
+  // ---- last CTA: per-row argmax, then acceptance and trim.  Every load of a
+  // phase is issued at once (one element per thread, block-strided) and the
+  // per-row / per-request results meet in shared memory, so the tail costs a
+  // few memory round trips instead of one per row.
   __threadfence();
-  const int lane = tid & 31;
-  for (int tt = tid >> 5; tt < T; tt += kGreedyThreads / 32) {
-    unsigned long long best = 0ull;
-    const unsigned long long* kr = keys + (long long)tt * nchunks;
-    for (int j = lane; j < nchunks; j += 32) {
-      const unsigned long long x = __ldcg(kr + j);
-      best = x > best ? x : best;
+  if (T <= kTailRows && R <= kTailRows) {
+    for (int tt = tid; tt < T; tt += kGreedyThreads) s_key[tt] = 0ull;
+    for (int r = tid; r < R; r += kGreedyThreads) s_n[r] = k;
+    __syncthreads();
+    const long long nk = (long long)T * nchunks;
+    for (long long f = tid; f < nk; f += kGreedyThreads)
+      atomicMax(&s_key[f / nchunks], __ldcg(keys + f));
+    __syncthreads();
+    for (int tt = tid; tt < T; tt += kGreedyThreads) {
+      const int a = (int)(0xFFFFFFFFu - (uint32_t)(s_key[tt] & 0xFFFFFFFFull));
+      s_arg[tt] = a;
+      argmax_ids[tt] = a;
     }
-    best = warp_max_u64(best);
-    if (lane == 0) argmax_ids[tt] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
-  }
-  __syncthreads();
-  for (int r = tid; r < R; r += kGreedyThreads) {
-    const int base = r * (k + 1);
-    int n = 0;
-    while (n < k && __ldg(draft_tokens + (long long)r * k + n) == argmax_ids[base + n]) ++n;
-    accepted[r] = n;
-    next_tokens[r] = argmax_ids[base + n];
-    kv_lens_out[r] = kv_lens_in[r] - (k - n);
+    __syncthreads();
+    const long long nd = (long long)R * k;
+    for (long long f = tid; f < nd; f += kGreedyThreads) {
+      const int r = (int)(f / k), j = (int)(f % k);
+      if (__ldg(draft_tokens + f) != s_arg[r * (k + 1) + j]) atomicMin(&s_n[r], j);
+    }
+    __syncthreads();
+    for (int r = tid; r < R; r += kGreedyThreads) {
+      const int n = s_n[r];
+      accepted[r] = n;
+      next_tokens[r] = s_arg[r * (k + 1) + n];
+      kv_lens_out[r] = kv_lens_in[r] - (k - n);
+    }
+  } else {
+    const int lane = tid & 31;
+    for (int tt = tid >> 5; tt < T; tt += kGreedyThreads / 32) {
+      unsigned long long best = 0ull;
+      const unsigned long long* kr = keys + (long long)tt * nchunks;
+      for (int j = lane; j < nchunks; j += 32) {
+        const unsigned long long x = __ldcg(kr + j);
+        best = x > best ? x : best;
+      }
+      best = warp_max_u64(best);
+      if (lane == 0) argmax_ids[tt] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+    }
+    __syncthreads();
+    __threadfence_block();
+    for (int r = tid; r < R; r += kGreedyThreads) {
+      const int base = r * (k + 1);
+      int n = 0;
+      while (n < k && __ldg(draft_tokens + (long long)r * k + n) == __ldcg(argmax_ids + base + n)) ++n;
+      accepted[r] = n;
+      next_tokens[r] = __ldcg(argmax_ids + base + n);
+      kv_lens_out[r] = kv_lens_in[r] - (k - n);
+    }
   }
   if (tid == 0) *ticket = 0u;  // leave the workspace zeroed for the next call
 }

@@ -111,3 +111,25 @@ def test_kv_append_host_checks(lib):
     assert f(4096, 4096, 4096, 0, 4, 2, 4096, 4, 64, None, None) == 0   # nothing to do
     assert f(None, 4096, 4096, 2, 4, 2, 4096, 4, 64, None, None) == 1
     assert f(4096 + 8, 4096, 4096, 2, 4, 2, 4096, 4, 64, None, None) == 3
+
+
+def test_sampled_host_checks(lib):
+    f = lib.spec_verify_sampled
+    fl = ctypes.c_float
+    ws = lib.sv_sampled_workspace_bytes(2, 3, 1000)
+    assert ws >= 256
+    args = [4096, 2, 3, 1000, fl(1.0), 4096, 4096, 4096, 4096, 4096, 4096, 4096, 4096, ws, None]
+    bad = list(args); bad[4] = fl(0.0)
+    assert f(*bad) == 2                     # temperature must be > 0
+    bad = list(args); bad[4] = fl(float("inf"))
+    assert f(*bad) == 2
+    bad = list(args); bad[3] = 0
+    assert f(*bad) == 2                     # V >= 1
+    bad = list(args); bad[1] = 0
+    assert f(*bad) == 0                     # no requests: nothing to do
+    bad = list(args); bad[6] = None
+    assert f(*bad) == 1                     # draft_probs needed when k > 0
+    bad = list(args); bad[13] = ws - 1
+    assert f(*bad) == 4
+    bad = list(args); bad[12] = 4096 + 16
+    assert f(*bad) == 3                     # workspace 256-byte aligned
