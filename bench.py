@@ -374,7 +374,9 @@ def main():
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic(args.config)
-    roof["kernel"] = "mla_verify_decode call (attention kernel" + (" + LSE combine)" if step.num_splits > 1 else ")")
+    roof["kernel"] = "mla_verify_decode call (" + {3: "plan + attention + LSE combine kernels",
+                                                   2: "attention + LSE combine kernels",
+                                                   1: "attention kernel"}[step.attention_launches] + ")"
     roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json burst)" if peak_kind == "measured" else "fallback"
     roof["algorithmic_per_launch"] = {"flops": attn_flops, "bytes": attn_bytes}
 
@@ -414,8 +416,8 @@ def main():
         "e2e": {"value": e2e_mean * 1000.0, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * step.launches_per_step,
-        "gpu_launches_all_timed_loops": args.steps * (2 * step.launches_per_step + 1 + 1
-                                                       + (1 if step.num_splits > 1 else 0) + 1 + 2),
+        "gpu_launches_all_timed_loops": args.steps * (2 * step.launches_per_step + step.attention_launches
+                                                       + 1 + 1 + 2),
         "clocks": clocks,
         "status_word": int(step.status.item()),
     }

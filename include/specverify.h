@@ -63,6 +63,8 @@ typedef enum {
 #define SV_LATENT_DIM 512
 #define SV_PAGE_SIZE 64
 #define SV_MAX_SPLITS 64
+/* num_splits value selecting the balanced split plan (see mla_verify_decode). */
+#define SV_SPLITS_BALANCED (-1)
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* sv_status_string(sv_status s);
@@ -100,18 +102,28 @@ const char* sv_status_string(sv_status s);
  *   gate          bf16 [T][H][512].
  *   H             heads, >= 1.
  *   softmax_scale scale of the scores (finite, > 0).
- *   num_splits    KV splits per (request, row tile): 0 = automatic, else
- *                 1..SV_MAX_SPLITS.  Split s of request r covers KV tiles
- *                 [s*n_r/S, (s+1)*n_r/S) (integer division) with
- *                 n_r = ceil(max_t kv_bounds[t] / 64) over r's tokens.
+ *   num_splits    how the KV of each request is cut into work units:
+ *                 1..SV_MAX_SPLITS: S uniform splits per (request, row tile);
+ *                   split s of request r covers KV tiles
+ *                   [s*n_r/S, (s+1)*n_r/S) (integer division) with
+ *                   n_r = ceil(max_t kv_bounds[t] / 64) over r's tokens.
+ *                 SV_SPLITS_BALANCED (-1): a plan computed on the device from
+ *                   kv_bounds cuts every request into pieces of c pages,
+ *                   c = max(ceil(sum_r n_r * n_tiles / SMs), ceil(max_r n_r / 64))
+ *                   (n_tiles = 128-row tiles per request), so that requests of
+ *                   very different lengths give the SMs equal work; the
+ *                   pieces run longest first.  One extra small kernel.
+ *                 0: automatic (sv_mla_verify_num_splits).
+ *                 The result does not depend on the choice beyond rounding.
  *   workspace     device scratch of at least
- *                 sv_mla_verify_workspace_bytes(T, H, S) bytes (S = the split
- *                 count used; sv_mla_verify_num_splits gives the automatic
- *                 one), 256-byte aligned; may be NULL when S == 1.  Holds the
- *                 split partials, layout part_o fp32 [S][T][H][512] followed
- *                 by part_lse fp32 [S][T][H] (lse of the split's KV range,
- *                 natural log, -inf for an empty range; part_o normalised
- *                 within the split, 0 for an empty range).
+ *                 sv_mla_verify_workspace_bytes(T, H, S) bytes (S = the
+ *                 num_splits used, after resolving 0), 256-byte aligned; may
+ *                 be NULL when S == 1.  With 2..SV_MAX_SPLITS uniform splits
+ *                 it holds the split partials: part_o fp32 [S][T][H][512]
+ *                 followed by part_lse fp32 [S][T][H] (lse of the split's KV
+ *                 range, natural log, -inf for an empty range; part_o
+ *                 normalised within the split, 0 for an empty range).  With
+ *                 the balanced plan its layout is internal.
  *   workspace_bytes  its size in bytes.
  *   out           bf16 [T][H][512] (round to nearest even).
  *   lse           fp32 [T][H], natural log of the ungated scaled scores.
@@ -119,8 +131,13 @@ const char* sv_status_string(sv_status s);
  *   stream        CUDA stream.
  * Returns SV_OK after enqueueing, or the first failed check.
  * ---------------------------------------------------------------------- */
-/* The split count num_splits = 0 resolves to on the current device (it only
- * looks at the sizes, never at device data). */
+/* The num_splits that 0 resolves to on the current device (it only looks at
+ * the sizes, never at device data): SV_SPLITS_BALANCED when R >= 2,
+ * max_pages_per_req >= 64 and 2 * ceil(H*q_per_req/128) * R <= SMs (long
+ * contexts whose units fit the SMs once), else a uniform count that fills the
+ * SMs once with >= 4 KV tiles per split.
+ * sv_mla_verify_workspace_bytes accepts any num_splits value mla_verify_decode
+ * accepts except 0 (resolve it first). */
 int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pages_per_req);
 size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits);
 

@@ -8,6 +8,7 @@ from .binding import (  # noqa: F401
     SV_DEV_BAD_BOUND,
     SV_DEV_BAD_PAGE,
     SV_DEV_TIMEOUT,
+    SV_SPLITS_BALANCED,
     SpecVerifyError,
     attention_workspace_bytes,
     greedy_workspace,

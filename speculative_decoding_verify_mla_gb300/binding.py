@@ -24,6 +24,7 @@ _c_void_p = ctypes.c_void_p
 SV_LATENT_DIM = 512
 SV_PAGE_SIZE = 64
 SV_MAX_SPLITS = 64
+SV_SPLITS_BALANCED = -1
 SV_DEV_BAD_PAGE = 0x1
 SV_DEV_BAD_BOUND = 0x2
 SV_DEV_TIMEOUT = 0x4

@@ -25,10 +25,15 @@ namespace {
 
 constexpr int kCombineThreads = 256;
 
+// Partial addressing.  Uniform splits: split s of row `row` is slot s, row
+// `row` of a [S][rows] table.  Balanced plan (plan_splits != NULL): request r
+// = row / Mq owns slots plan_base[r] .. + plan_splits[r] - 1 of a [slots][Mq]
+// table, and a request with one piece was finished by the attention kernel.
 __global__ void __launch_bounds__(kCombineThreads)
     lse_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
-                       int S, long long rows, const __nv_bfloat16* __restrict__ gate,
-                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
+                       int S_uniform, long long rows, const __nv_bfloat16* __restrict__ gate,
+                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out,
+                       const int* plan_splits, const int* plan_base, int Mq) {
   // one warp per half row (256 columns): lane owns columns 128j + 4 lane .. +3, j = 0, 1
   const int lane = threadIdx.x & 31;
   const long long hrow = (long long)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
@@ -44,10 +49,21 @@ __global__ void __launch_bounds__(kCombineThreads)
   // launch), wait here until its partials are complete and visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
+  int S = S_uniform;
+  long long slot0 = 0, slot_rows = rows, rin = row;
+  if (plan_splits) {
+    const long long rq = row / Mq;
+    S = ld_dep_s32(plan_splits + rq);
+    if (S < 2) return;  // finished by the attention kernel
+    slot0 = ld_dep_s32(plan_base + rq);
+    slot_rows = Mq;
+    rin = row - rq * Mq;
+  }
+
   // split weights: lane s holds lse_s for s = lane and lane + 32
   float l0 = -INFINITY, l1 = -INFINITY;
-  if (lane < S) l0 = ld_dep_f32(part_lse + (long long)lane * rows + row);
-  if (lane + 32 < S) l1 = ld_dep_f32(part_lse + (long long)(lane + 32) * rows + row);
+  if (lane < S) l0 = ld_dep_f32(part_lse + (slot0 + lane) * slot_rows + rin);
+  if (lane + 32 < S) l1 = ld_dep_f32(part_lse + (slot0 + lane + 32) * slot_rows + rin);
   float m = fmaxf(l0, l1);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -70,7 +86,7 @@ __global__ void __launch_bounds__(kCombineThreads)
       for (int u = 0; u < 8; ++u) {
         const int s = s0 + u;
         ws[u] = (s < S) ? __shfl_sync(0xFFFFFFFFu, s < 32 ? w0 : w1, s & 31) * inv_z : 0.f;
-        const float* src = part_o + ((long long)min(s, S - 1) * rows + row) * 512 + col0;
+        const float* src = part_o + ((slot0 + min(s, S - 1)) * slot_rows + rin) * 512 + col0;
 #pragma unroll
         for (int j = 0; j < 2; ++j)
           v[u][j] = (ws[u] != 0.f) ? ld_dep_f4_stream(reinterpret_cast<const float4*>(src + 128 * j))
@@ -106,7 +122,8 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 // Internal launcher shared with mla_verify_decode (no argument checks).
 cudaError_t launch_lse_combine(const float* part_o, const float* part_lse, int S, long long rows,
-                               const void* gate, void* out, float* lse, cudaStream_t stream) {
+                               const void* gate, void* out, float* lse, cudaStream_t stream,
+                               const int* plan_splits, const int* plan_base, int Mq) {
   if (rows == 0) return cudaSuccess;
   const long long blocks = (2 * rows + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
   // programmatic dependent launch: the grid may start while the previous
@@ -123,7 +140,8 @@ cudaError_t launch_lse_combine(const float* part_o, const float* part_lse, int S
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, lse_combine_kernel, part_o, part_lse, S, rows,
                                            static_cast<const __nv_bfloat16*>(gate),
-                                           static_cast<__nv_bfloat16*>(out), lse);
+                                           static_cast<__nv_bfloat16*>(out), lse, plan_splits,
+                                           plan_base, Mq);
   if (e != cudaSuccess) cudaGetLastError();
   return e;
 }
@@ -144,7 +162,8 @@ extern "C" sv_status mla_lse_combine(const float* part_o, const float* part_lse,
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return SV_ERR_ALIGN;
   return sv::launch_lse_combine(part_o, part_lse, S, rows, gate, out, lse,
-                                reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+                                reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr,
+                                1) == cudaSuccess
              ? SV_OK
              : SV_ERR_LAUNCH;
 }

@@ -53,7 +53,8 @@
 namespace sv {
 
 cudaError_t launch_lse_combine(const float* part_o, const float* part_lse, int S, long long rows,
-                               const void* gate, void* out, float* lse, cudaStream_t stream);
+                               const void* gate, void* out, float* lse, cudaStream_t stream,
+                               const int* plan_splits, const int* plan_base, int Mq);
 
 namespace {
 
@@ -99,6 +100,11 @@ struct VerifyParams {
   long long rows_total;  // T * H
   int R, q_per_req, H, max_pages, num_pages, num_splits, n_mtiles;
   float scale_log2;  // softmax_scale * log2(e)
+  // balanced plan (units != nullptr): unit list and header written by the
+  // plan kernel, the prerequisite grid of this launch
+  const int4* units;
+  const int* plan_header;
+  long long part_w_stride;  // part_lse elements between consecutive slots
 };
 
 __device__ __forceinline__ int load_bound(const VerifyParams& p, int tok) {
@@ -158,13 +164,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int half = blockIdx.x & 1;  // latent half of O owned by this CTA
-  const int unit = blockIdx.x >> 1;
+  // ---- the work unit: (request r, 128-row tile, latent half, KV tile range)
+  int half, m_tile, r, s_idx = 0, plan_lo = 0, plan_hi = 0, slot = -1;
+  bool fused;  // one piece: normalise + gate here, else write a partial
   const int S = p.num_splits;
-  const int s_idx = unit % S;
-  const int rm = unit / S;
-  const int m_tile = rm % p.n_mtiles;
-  const int r = rm / p.n_mtiles;
+  if (p.units) {
+    // balanced plan: wait for the plan kernel, then read this CTA's unit
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if ((int)blockIdx.x >= ld_dep_s32(p.plan_header + 1)) return;  // spare CTA
+    const int4 u = ld_dep_i4(p.units + blockIdx.x);
+    r = u.x;
+    m_tile = u.y >> 1;
+    half = u.y & 1;
+    plan_lo = u.z & 0xFFFF;
+    plan_hi = (int)((unsigned)u.z >> 16);
+    slot = u.w;
+    fused = slot < 0;
+  } else {
+    half = blockIdx.x & 1;  // latent half of O owned by this CTA
+    const int unit = blockIdx.x >> 1;
+    s_idx = unit % S;
+    const int rm = unit / S;
+    m_tile = rm % p.n_mtiles;
+    r = rm / p.n_mtiles;
+    fused = (S == 1);
+  }
   const int Mq = p.H * p.q_per_req;
 
   // warp 0: start the dependent loads of the set-up (bounds -> block table ->
@@ -216,16 +240,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   // ---- unit geometry (every thread derives the same values)
-  int maxb_req = 0;
-  for (int t = 0; t < p.q_per_req; ++t) maxb_req = max(maxb_req, load_bound(p, r * p.q_per_req + t));
   const int t_first = (m_tile * kMTile) / p.H;
   const int t_last = min((m_tile * kMTile + kMTile - 1) / p.H, p.q_per_req - 1);
   int maxb_tile = 0;
   for (int t = t_first; t <= t_last; ++t)
     maxb_tile = max(maxb_tile, load_bound(p, r * p.q_per_req + t));
-  const int n_r = (maxb_req + kTileN - 1) / kTileN;
-  const int lo = (int)((long long)s_idx * n_r / S);
-  const int hi = (int)((long long)(s_idx + 1) * n_r / S);
+  int lo = plan_lo, hi = plan_hi;
+  if (!p.units) {
+    int maxb_req = 0;
+    for (int t = 0; t < p.q_per_req; ++t)
+      maxb_req = max(maxb_req, load_bound(p, r * p.q_per_req + t));
+    const int n_r = (maxb_req + kTileN - 1) / kTileN;
+    lo = (int)((long long)s_idx * n_r / S);
+    hi = (int)((long long)(s_idx + 1) * n_r / S);
+  }
   const int hi_eff = min(hi, (maxb_tile + kTileN - 1) / kTileN);
   const int ntiles = max(0, hi_eff - lo);
 
@@ -378,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_loc = valid ? f / p.H : 0;
     const long long row_g = (long long)r * Mq + f;
     const int b_i = valid ? load_bound(p, r * p.q_per_req + t_loc) : 0;
-    const bool fused_gate = (S == 1);
+    const bool fused_gate = fused;
 
     if (ntiles > 0) {
       // this CTA's half of the query row -> TMEM (bf16 pairs per 32-bit column)
@@ -545,7 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                           __uint_as_float(v[4 * u + 2]) * inv_l, __uint_as_float(v[4 * u + 3]) * inv_l);
         }
       }
-      if (valid && half == 0) p.part_lse[(long long)s_idx * p.rows_total + row_g] = lse_v;
+      if (valid && half == 0) {
+        const long long w = p.units ? slot : s_idx;
+        const long long z = p.units ? 0 : r;
+        p.part_lse[w * p.part_w_stride + z * Mq + f] = lse_v;
+      }
     }
     fence_proxy_async_smem();
     named_bar_sync(kEpilogueBarId, 128);
@@ -558,8 +590,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
 #pragma unroll
         for (int b = 0; b < 8; ++b)
-          tma_store_4d(&tmap_part, st0 + b * kQBoxBytes, half * kDHalf + b * 32, m_tile * kMTile, r,
-                       s_idx);
+          tma_store_4d(&tmap_part, st0 + b * kQBoxBytes, half * kDHalf + b * 32, m_tile * kMTile,
+                       p.units ? 0 : r, p.units ? slot : s_idx);
       }
       tma_store_commit();
       tma_store_wait_read();  // SMEM stays valid until the stores have read it
@@ -573,6 +605,171 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ balanced plan
+// One CTA turns the per-token bounds into the unit list of the attention
+// kernel.  Request r needs n_r = ceil(max_t b_t / 64) KV tiles; with n_mt row
+// tiles per request and two latent halves, the whole batch is
+// 2 * n_mt * sum_r n_r CTA-tiles of work.  Pieces of c tiles,
+//   c = max(ceil(sum_r n_r * n_mt / SMs), ceil(max_r n_r / SV_MAX_SPLITS)),
+// give about two units per SM; request r gets s_r = max(1, ceil(n_r / c))
+// pieces (the last one shorter).  Units are listed longest first (a counting
+// sort over piece lengths), so the block scheduler hands the long pieces out
+// before the short ones.  A request with one piece is finished by its units
+// (normalise + gate); the others write partials to slots plan_base[r] + j.
+// Layout of the plan area: header {c, n_units, n_slots}, splits[R],
+// base[R], units[units_max] (int4: r, m_tile << 1 | half, lo | hi << 16,
+// slot or -1).
+constexpr int kPlanThreads = 1024;
+constexpr int kLenBuckets = 1024;
+
+__device__ __forceinline__ int plan_bound(const int32_t* kv_bounds, int tok, int cap) {
+  const int b = __ldg(kv_bounds + tok);
+  return b < 0 ? 0 : (b > cap ? cap : b);
+}
+
+template <typename T>
+__device__ T block_reduce(T v, T* s_red, bool is_max) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const T x = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = is_max ? (x > v ? x : v) : v + x;
+  }
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = lane < nw ? s_red[lane] : (T)0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const T x = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+      v = is_max ? (x > v ? x : v) : v + x;
+    }
+    if (lane == 0) s_red[0] = v;
+  }
+  __syncthreads();
+  const T r = s_red[0];
+  __syncthreads();
+  return r;
+}
+
+// Exclusive prefix sum over the block (one value per thread, thread order).
+__device__ int block_excl_scan(int v, int* s_scan, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_scan[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? s_scan[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) s_scan[32 + lane] = w;
+  }
+  __syncthreads();
+  const int res = (warp > 0 ? s_scan[32 + warp - 1] : 0) + incl - v;
+  *total = s_scan[32 + nw - 1];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+    plan_kernel(const int32_t* __restrict__ kv_bounds, int R, int q_per_req, int max_pages,
+                int n_mt, int sms, int units_max, int slots_max, int* __restrict__ header,
+                int* __restrict__ splits, int* __restrict__ base, int4* __restrict__ units,
+                int32_t* __restrict__ status) {
+  __shared__ long long s_red64[32];
+  __shared__ int s_red[32];
+  __shared__ int s_scan[64];
+  __shared__ int s_cnt[kLenBuckets];
+  // the attention CTAs may take their SMs now; they wait for this grid
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x;
+  const int cap = max_pages * kTileN;
+  // 1. KV tiles per request (kept in `splits` until step 4)
+  long long psum = 0;
+  int pmax = 0;
+  for (int r = tid; r < R; r += kPlanThreads) {
+    int mb = 0;
+    for (int t = 0; t < q_per_req; ++t) mb = max(mb, plan_bound(kv_bounds, r * q_per_req + t, cap));
+    const int n = (mb + kTileN - 1) / kTileN;
+    splits[r] = n;
+    psum += n;
+    pmax = max(pmax, n);
+  }
+  psum = block_reduce<long long>(psum, s_red64, false);
+  pmax = block_reduce<int>(pmax, s_red, true);
+  long long c = (psum * n_mt + sms - 1) / sms;
+  c = max(c, (long long)(pmax + SV_MAX_SPLITS - 1) / SV_MAX_SPLITS);
+  if (c < 1) c = 1;
+  // 2. pieces per request, slots, and piece-length histogram
+  for (int b = tid; b < kLenBuckets; b += kPlanThreads) s_cnt[b] = 0;
+  __syncthreads();
+  int carry_slots = 0, carry_units = 0;
+  for (int r0 = 0; r0 < R; r0 += kPlanThreads) {
+    const int r = r0 + tid;
+    int n = 0, sr = 0;
+    if (r < R) {
+      n = splits[r];
+      sr = n == 0 ? 1 : (int)((n + c - 1) / c);
+      for (int j = 0; j < sr; ++j) {
+        const int len = (j < sr - 1) ? (int)c : n - (int)((sr - 1) * c);
+        const int bk = (int)((long long)len * (kLenBuckets - 1) / c);
+        atomicAdd(&s_cnt[bk], 2 * n_mt);
+      }
+    }
+    int tot = 0;
+    const int b_excl = block_excl_scan(sr >= 2 ? sr : 0, s_scan, &tot);
+    if (r < R) base[r] = carry_slots + b_excl;
+    carry_slots += tot;
+    int tu = 0;
+    block_excl_scan(sr, s_scan, &tu);
+    carry_units += tu * 2 * n_mt;
+  }
+  __syncthreads();
+  // 3. start of every length bucket, longest first (bucket kLenBuckets-1 first)
+  {
+    const int b = kLenBuckets - 1 - tid;  // thread tid owns the tid-th longest bucket
+    const int v = (tid < kLenBuckets) ? s_cnt[b] : 0;
+    int tot = 0;
+    const int st = block_excl_scan(v, s_scan, &tot);
+    if (tid < kLenBuckets) s_cnt[b] = st;
+  }
+  __syncthreads();
+  const bool fits = carry_units <= units_max && carry_slots <= slots_max;
+  if (!fits && tid == 0 && status) atomicOr(status, SV_DEV_BAD_BOUND);
+  // 4. place the units
+  for (int r = tid; fits && r < R; r += kPlanThreads) {
+    const int n = splits[r];
+    const int sr = n == 0 ? 1 : (int)((n + c - 1) / c);
+    for (int j = 0; j < sr; ++j) {
+      const int plo = (int)(j * c);
+      const int phi = (j < sr - 1) ? (int)((j + 1) * c) : n;
+      const int bk = (int)((long long)(phi - plo) * (kLenBuckets - 1) / c);
+      const int pos = atomicAdd(&s_cnt[bk], 2 * n_mt);
+      const int sl = sr >= 2 ? base[r] + j : -1;
+      for (int u = 0; u < 2 * n_mt; ++u)
+        units[pos + u] = make_int4(r, u, plo | (phi << 16), sl);
+    }
+  }
+  __syncthreads();
+  for (int r = tid; r < R; r += kPlanThreads) {
+    const int n = splits[r];
+    splits[r] = n == 0 ? 1 : (int)((n + c - 1) / c);
+  }
+  if (tid == 0) {
+    header[0] = (int)c;
+    header[1] = fits ? carry_units : 0;
+    header[2] = carry_slots;
   }
 }
 
@@ -650,22 +847,65 @@ inline bool misaligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0;
 }
 
+inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+int current_sm_count() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+    return v;
+  return 152;
+}
+
+// Balanced-plan workspace: header, splits[R], base[R], units, then the
+// partials of at most slots_max pieces ([slots][Mq][512] fp32 + [slots][Mq]).
+struct PlanLayout {
+  size_t splits, base, units, part_o, part_lse, total;
+  int units_max, slots_max;
+};
+PlanLayout plan_layout(int R, int Mq, int n_mt, int sms) {
+  PlanLayout L;
+  L.units_max = 2 * sms + 2 * n_mt * R;
+  L.slots_max = sms / n_mt + R + 1;
+  L.splits = 256;
+  L.base = L.splits + align256((size_t)R * 4);
+  L.units = L.base + align256((size_t)R * 4);
+  L.part_o = L.units + align256((size_t)L.units_max * 16);
+  L.part_lse = L.part_o + align256((size_t)L.slots_max * Mq * kD * 4);
+  L.total = L.part_lse + align256((size_t)L.slots_max * Mq * 4);
+  return L;
+}
+// An upper bound of plan_layout(...).total from T = R*q_per_req and H only
+// (n_mt * R <= T*H/128 + R, slots * Mq <= 128*sms + 2*T*H).
+size_t plan_workspace_bound(long long T, long long H, int sms) {
+  const long long rows = T * H;
+  const long long units_max = 2ll * sms + 2 * (rows / 128 + T);
+  const long long slot_rows = 128ll * sms + 2 * rows;
+  return 256 + 2 * align256((size_t)T * 4) + align256((size_t)units_max * 16) +
+         align256((size_t)slot_rows * kD * 4) + align256((size_t)slot_rows * 4) + 1024;
+}
+
 }  // namespace
 }  // namespace sv
 
+// Automatic choice.  A unit costs about 8 KV tiles of fixed set-up and
+// epilogue (measured on GB300: ~12 us against ~1.6 us per tile), so cutting
+// requests into pieces pays only for long contexts: the balanced plan is used
+// when the requests' row tiles fit the SMs once (so uniform splits would
+// leave SMs idle behind the longest request) and a request may hold at least
+// 64 tiles (4096 positions); otherwise uniform splits.
 extern "C" int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pages_per_req) {
-  int sms = 152;
-  int dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      sms = v;
-  }
+  const int sms = sv::current_sm_count();
+  const long long n_mt = ((long long)H * q_per_req + sv::kMTile - 1) / sv::kMTile;
+  if (R >= 2 && max_pages_per_req >= 64 && max_pages_per_req <= 0xFFFF && 2 * n_mt * R <= sms)
+    return SV_SPLITS_BALANCED;
   return sv::auto_splits(R, q_per_req, H, max_pages_per_req, sms);
 }
 
 extern "C" size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits) {
-  if (T <= 0 || H <= 0 || num_splits <= 1) return 0;
+  if (T <= 0 || H <= 0) return 0;
+  if (num_splits == SV_SPLITS_BALANCED) return sv::plan_workspace_bound(T, H, sv::current_sm_count());
+  if (num_splits <= 1) return 0;
   const size_t rows = (size_t)T * (size_t)H;
   const size_t o_bytes = (size_t)num_splits * rows * sv::kD * sizeof(float);
   return o_bytes + (size_t)num_splits * rows * sizeof(float);
@@ -682,7 +922,9 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
   if (R < 0 || q_per_req < 1 || H < 1 || max_pages_per_req < 0 || num_pages < 0)
     return SV_ERR_SHAPE;
   if (page_size != SV_PAGE_SIZE) return SV_ERR_UNSUPPORTED;
-  if (num_splits < 0 || num_splits > SV_MAX_SPLITS) return SV_ERR_SHAPE;
+  if ((num_splits < 0 && num_splits != SV_SPLITS_BALANCED) || num_splits > SV_MAX_SPLITS)
+    return SV_ERR_SHAPE;
+  if (num_splits == SV_SPLITS_BALANCED && max_pages_per_req > 0xFFFF) return SV_ERR_SHAPE;
   const long long T = (long long)R * q_per_req;
   if (T == 0) return SV_OK;
   if (T * H > 0x7FFFFFFFll || (long long)num_pages * kTileN > 0x7FFFFFFFll) return SV_ERR_SHAPE;
@@ -694,13 +936,29 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
       misaligned(out, 16) || misaligned(lse, 4) || misaligned(block_table, 4) ||
       misaligned(kv_bounds, 4))
     return SV_ERR_ALIGN;
+  if ((num_splits == SV_SPLITS_BALANCED || num_splits > 1) && !workspace) return SV_ERR_WORKSPACE;
   int sm_count = 0;
   if (!device_setup(&sm_count)) return SV_ERR_DEVICE;
-  const int S = num_splits > 0 ? num_splits
-                               : auto_splits(R, q_per_req, H, max_pages_per_req, sm_count);
+  const int S = num_splits != 0 ? num_splits
+                                : sv_mla_verify_num_splits(R, q_per_req, H, max_pages_per_req);
+  const bool balanced = (S == SV_SPLITS_BALANCED);
+  const long long Mq_ll = (long long)H * q_per_req;
+  const int n_mt = (int)((Mq_ll + kMTile - 1) / kMTile);
   float* part_o = nullptr;
   float* part_lse = nullptr;
-  if (S > 1) {
+  PlanLayout PL{};
+  char* plan_base_ptr = nullptr;
+  if (balanced) {
+    if (!workspace) return SV_ERR_WORKSPACE;
+    if (misaligned(workspace, 256)) return SV_ERR_ALIGN;
+    PL = plan_layout(R, (int)Mq_ll, n_mt, sm_count);
+    if (workspace_bytes < PL.total ||
+        workspace_bytes < sv_mla_verify_workspace_bytes((int)T, H, SV_SPLITS_BALANCED))
+      return SV_ERR_WORKSPACE;
+    plan_base_ptr = static_cast<char*>(workspace);
+    part_o = reinterpret_cast<float*>(plan_base_ptr + PL.part_o);
+    part_lse = reinterpret_cast<float*>(plan_base_ptr + PL.part_lse);
+  } else if (S > 1) {
     if (!workspace) return SV_ERR_WORKSPACE;
     if (misaligned(workspace, 256)) return SV_ERR_ALIGN;
     if (workspace_bytes < sv_mla_verify_workspace_bytes((int)T, H, S)) return SV_ERR_WORKSPACE;
@@ -721,7 +979,12 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
         !encode_map(&tmap_gate, bf16, 2, gate, 3, row_dims, row_box) ||
         !encode_map(&tmap_out, bf16, 2, out, 3, row_dims, row_box))
       return SV_ERR_ALIGN;
-    if (S > 1) {
+    if (balanced) {
+      const cuuint64_t part_dims[4] = {(cuuint64_t)kD, (cuuint64_t)Mq, 1, (cuuint64_t)PL.slots_max};
+      const cuuint32_t part_box[4] = {32, (cuuint32_t)kMTile, 1, 1};
+      if (!encode_map(&tmap_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, part_o, 4, part_dims, part_box))
+        return SV_ERR_ALIGN;
+    } else if (S > 1) {
       const cuuint64_t part_dims[4] = {(cuuint64_t)kD, (cuuint64_t)Mq, (cuuint64_t)R, (cuuint64_t)S};
       const cuuint32_t part_box[4] = {32, (cuuint32_t)kMTile, 1, 1};
       if (!encode_map(&tmap_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, part_o, 4, part_dims, part_box))
@@ -748,20 +1011,56 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
   prm.max_pages = max_pages_per_req;
   prm.num_pages = num_pages;
   prm.num_splits = S;
-  prm.n_mtiles = (int)(((long long)H * q_per_req + kMTile - 1) / kMTile);
+  prm.n_mtiles = n_mt;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
+  prm.units = nullptr;
+  prm.plan_header = nullptr;
+  prm.part_w_stride = T * H;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-  const long long ctas = 2ll * R * prm.n_mtiles * S;
-  if (ctas > 0x7FFFFFFFll) return SV_ERR_SHAPE;
-  mla_verify_kernel<<<(unsigned)ctas, kThreads, kSmemBytes,
-                      reinterpret_cast<cudaStream_t>(stream)>>>(tmap_kv, tmap_q, tmap_gate, tmap_out,
-                                                                tmap_part, prm);
-  if (cudaGetLastError() != cudaSuccess) return SV_ERR_LAUNCH;
-  if (S > 1) {
-    if (launch_lse_combine(part_o, part_lse, S, T * H, gate, out, lse,
-                           reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (!balanced) {
+    const long long ctas = 2ll * R * prm.n_mtiles * S;
+    if (ctas > 0x7FFFFFFFll) return SV_ERR_SHAPE;
+    mla_verify_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(tmap_kv, tmap_q, tmap_gate,
+                                                                   tmap_out, tmap_part, prm);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_LAUNCH;
+    if (S > 1 && launch_lse_combine(part_o, part_lse, S, T * H, gate, out, lse, st, nullptr,
+                                    nullptr, 1) != cudaSuccess)
       return SV_ERR_LAUNCH;
+    return SV_OK;
   }
+
+  // balanced plan: plan kernel, then the attention kernel and the merge, each
+  // a programmatic dependent launch of the one before
+  int* header = reinterpret_cast<int*>(plan_base_ptr);
+  int* splits = reinterpret_cast<int*>(plan_base_ptr + PL.splits);
+  int* pbase = reinterpret_cast<int*>(plan_base_ptr + PL.base);
+  int4* units = reinterpret_cast<int4*>(plan_base_ptr + PL.units);
+  plan_kernel<<<1, kPlanThreads, 0, st>>>(kv_bounds, R, q_per_req, max_pages_per_req, n_mt,
+                                          sm_count, PL.units_max, PL.slots_max, header, splits,
+                                          pbase, units, status);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_LAUNCH;
+  prm.units = units;
+  prm.plan_header = header;
+  prm.part_w_stride = Mq_ll;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)PL.units_max, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, mla_verify_kernel, tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part,
+                         prm) != cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_LAUNCH;
+  }
+  if (launch_lse_combine(part_o, part_lse, 0, T * H, gate, out, lse, st, splits, pbase,
+                         (int)Mq_ll) != cudaSuccess)
+    return SV_ERR_LAUNCH;
   return SV_OK;
 }
 

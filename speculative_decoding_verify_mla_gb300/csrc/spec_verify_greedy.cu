@@ -26,7 +26,6 @@ namespace {
 
 constexpr int kGreedyThreads = 256;
 constexpr size_t kGreedyHeader = 256;  // ticket counter, padded
-constexpr int kTailRows = 1024;        // rows / requests the shared-memory tail handles
 
 __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
   uint32_t u = __float_as_uint(v);
@@ -60,11 +59,11 @@ __global__ void __launch_bounds__(kGreedyThreads)
                          const int32_t* __restrict__ kv_lens_in, int32_t* __restrict__ argmax_ids,
                          int32_t* __restrict__ accepted, int32_t* __restrict__ next_tokens,
                          int32_t* __restrict__ kv_lens_out, unsigned int* __restrict__ ticket,
-                         unsigned long long* __restrict__ keys) {
+                         unsigned long long* __restrict__ keys, unsigned long long* row_key,
+                         int* n_acc) {
+  // Shared memory stays under 1 KB so that this kernel can share an SM with
+  // the attention kernel (which leaves ~1.8 KB of the SM's shared memory).
   __shared__ unsigned long long s_warp[kGreedyThreads / 32];
-  __shared__ unsigned long long s_key[kTailRows];
-  __shared__ int s_arg[kTailRows];
-  __shared__ int s_n[kTailRows];
   __shared__ bool s_last;
   const int tid = threadIdx.x;
   const long long bid = blockIdx.x;
@@ -129,58 +128,77 @@ __global__ void __launch_bounds__(kGreedyThreads)
   if (!s_last) return;
 
   // ---- last CTA: per-row argmax, then acceptance and trim.  Every load of a
-  // phase is issued at once (one element per thread, block-strided) and the
-  // per-row / per-request results meet in shared memory, so the tail costs a
-  // few memory round trips instead of one per row.
+  // phase is issued at once (block-strided, one element per thread) and the
+  // per-row / per-request results meet through L2 atomics on workspace slots,
+  // so the tail costs a few memory round trips instead of one per row.
+  // Global writes and atomics of this block are visible to all its threads
+  // after __syncthreads; the reads go to L2 (.cg).
   __threadfence();
-  if (T <= kTailRows && R <= kTailRows) {
-    for (int tt = tid; tt < T; tt += kGreedyThreads) s_key[tt] = 0ull;
-    for (int r = tid; r < R; r += kGreedyThreads) s_n[r] = k;
-    __syncthreads();
-    const long long nk = (long long)T * nchunks;
-    for (long long f = tid; f < nk; f += kGreedyThreads)
-      atomicMax(&s_key[f / nchunks], __ldcg(keys + f));
-    __syncthreads();
-    for (int tt = tid; tt < T; tt += kGreedyThreads) {
-      const int a = (int)(0xFFFFFFFFu - (uint32_t)(s_key[tt] & 0xFFFFFFFFull));
-      s_arg[tt] = a;
-      argmax_ids[tt] = a;
-    }
-    __syncthreads();
-    const long long nd = (long long)R * k;
-    for (long long f = tid; f < nd; f += kGreedyThreads) {
-      const int r = (int)(f / k), j = (int)(f % k);
-      if (__ldg(draft_tokens + f) != s_arg[r * (k + 1) + j]) atomicMin(&s_n[r], j);
-    }
-    __syncthreads();
-    for (int r = tid; r < R; r += kGreedyThreads) {
-      const int n = s_n[r];
-      accepted[r] = n;
-      next_tokens[r] = s_arg[r * (k + 1) + n];
-      kv_lens_out[r] = kv_lens_in[r] - (k - n);
-    }
-  } else {
-    const int lane = tid & 31;
-    for (int tt = tid >> 5; tt < T; tt += kGreedyThreads / 32) {
+  if (T <= 32) {
+    // small batch: one warp, lane t owns row t; the keys and the drafts are
+    // loaded at once, a ballot marks the mismatching drafts and a shuffle
+    // fetches each request's next token (two memory round trips)
+    if (tid < 32) {
+      const int t = tid;
+      const bool row = t < T;
+      const int rq = row ? t / (k + 1) : 0;
+      const int j = row ? t % (k + 1) : 0;
+      const int d = (row && j < k) ? __ldg(draft_tokens + (long long)rq * k + j) : -1;
       unsigned long long best = 0ull;
-      const unsigned long long* kr = keys + (long long)tt * nchunks;
-      for (int j = lane; j < nchunks; j += 32) {
-        const unsigned long long x = __ldcg(kr + j);
-        best = x > best ? x : best;
+      if (row) {
+        const unsigned long long* kr = keys + (long long)t * nchunks;
+        int c2 = 0;
+        for (; c2 + 4 <= nchunks; c2 += 4) {
+          unsigned long long v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v[u] = __ldcg(kr + c2 + u);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) best = v[u] > best ? v[u] : best;
+        }
+        for (; c2 < nchunks; ++c2) {
+          const unsigned long long v = __ldcg(kr + c2);
+          best = v > best ? v : best;
+        }
       }
-      best = warp_max_u64(best);
-      if (lane == 0) argmax_ids[tt] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+      const int a = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+      if (row) argmax_ids[t] = a;
+      const unsigned mis = __ballot_sync(0xFFFFFFFFu, row && j < k && d != a);
+      int n = k;
+      if (t < R && k > 0) {
+        const unsigned seg = (mis >> (t * (k + 1))) & (k >= 32 ? 0xFFFFFFFFu : ((1u << k) - 1u));
+        n = seg ? __ffs(seg) - 1 : k;
+      }
+      const int nxt = __shfl_sync(0xFFFFFFFFu, a, t < R ? t * (k + 1) + n : 0);
+      if (t < R) {
+        accepted[t] = n;
+        next_tokens[t] = nxt;
+        kv_lens_out[t] = kv_lens_in[t] - (k - n);
+      }
     }
-    __syncthreads();
-    __threadfence_block();
-    for (int r = tid; r < R; r += kGreedyThreads) {
-      const int base = r * (k + 1);
-      int n = 0;
-      while (n < k && __ldg(draft_tokens + (long long)r * k + n) == __ldcg(argmax_ids + base + n)) ++n;
-      accepted[r] = n;
-      next_tokens[r] = __ldcg(argmax_ids + base + n);
-      kv_lens_out[r] = kv_lens_in[r] - (k - n);
-    }
+    if (tid == 0) *ticket = 0u;
+    return;
+  }
+  for (int tt = tid; tt < T; tt += kGreedyThreads) row_key[tt] = 0ull;
+  for (int r = tid; r < R; r += kGreedyThreads) n_acc[r] = k;
+  __syncthreads();
+  const long long nk = (long long)T * nchunks;
+  for (long long f = tid; f < nk; f += kGreedyThreads)
+    atomicMax(row_key + f / nchunks, __ldcg(keys + f));
+  __syncthreads();
+  for (int tt = tid; tt < T; tt += kGreedyThreads)
+    argmax_ids[tt] = (int32_t)(0xFFFFFFFFu - (uint32_t)(__ldcg(row_key + tt) & 0xFFFFFFFFull));
+  __syncthreads();
+  const long long nd = (long long)R * k;
+  for (long long f = tid; f < nd; f += kGreedyThreads) {
+    const int r = (int)(f / k), j = (int)(f % k);
+    if (__ldg(draft_tokens + f) != __ldcg(argmax_ids + r * (k + 1) + j)) atomicMin(n_acc + r, j);
+  }
+  __syncthreads();
+  for (int r = tid; r < R; r += kGreedyThreads) {
+    const int n = __ldcg(n_acc + r);
+    accepted[r] = n;
+    next_tokens[r] = __ldcg(argmax_ids + r * (k + 1) + n);
+    kv_lens_out[r] = kv_lens_in[r] - (k - n);
   }
   if (tid == 0) *ticket = 0u;  // leave the workspace zeroed for the next call
 }
@@ -199,11 +217,14 @@ int greedy_chunk(int T, int V) {
 }  // namespace
 }  // namespace sv
 
+// Workspace: ticket header, then the chunk keys [T][nchunks], the per-row
+// keys [T] and the per-request accept counts [T >= R] of the tail.
 extern "C" size_t sv_greedy_workspace_bytes(int T, int V) {
   if (T <= 0 || V <= 0) return sv::kGreedyHeader;
   const int chunk = sv::greedy_chunk(T, V);
   const long long nchunks = (V + (long long)chunk - 1) / chunk;
-  return sv::kGreedyHeader + (size_t)T * (size_t)nchunks * sizeof(unsigned long long);
+  return sv::kGreedyHeader + (size_t)T * (size_t)nchunks * sizeof(unsigned long long) +
+         (size_t)T * sizeof(unsigned long long) + (size_t)T * sizeof(int);
 }
 
 extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R, int k,
@@ -232,10 +253,12 @@ extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R
   auto* ticket = reinterpret_cast<unsigned int*>(workspace);
   auto* keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
                                                      sv::kGreedyHeader);
+  auto* row_key = keys + (size_t)T * nchunks;
+  auto* n_acc = reinterpret_cast<int*>(row_key + T);
   sv::greedy_verify_kernel<<<(unsigned)blocks, sv::kGreedyThreads, 0,
                              reinterpret_cast<cudaStream_t>(stream)>>>(
       logits, T, V, R, k, chunk, nchunks, vec4, draft_tokens, kv_lens_in, argmax_ids, accepted,
-      next_tokens, kv_lens_out, ticket, keys);
+      next_tokens, kv_lens_out, ticket, keys, row_key, n_acc);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_LAUNCH;
 }
 

@@ -40,8 +40,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr size_t kAlign = 256;
 constexpr int kStage = 1024;  // chunk totals staged per pass in the draw kernel
-constexpr int kTailStats = 2048;  // chunk statistics the shared-memory tail stages
-constexpr int kTailRows = 1024;   // rows / requests the shared-memory tail handles
+
 
 struct Decision {
   int n;      // accepted drafts
@@ -107,7 +106,7 @@ int draw_chunk_bulk(int R, int V) {
 }
 
 struct Layout {
-  size_t tickets2, stats, rowstat, decisions, sums, total;
+  size_t tickets2, stats, rowstat, decisions, sums, nacc, total;
   int chunk1, nch1, chunk2, nch2;
 };
 Layout layout(int R, int k, int V, bool bulk) {
@@ -122,7 +121,8 @@ Layout layout(int R, int k, int V, bool bulk) {
   L.rowstat = L.stats + align_up((size_t)T * L.nch1 * sizeof(float2));
   L.decisions = L.rowstat + align_up((size_t)T * sizeof(float2));
   L.sums = L.decisions + align_up((size_t)R * sizeof(Decision));
-  L.total = L.sums + align_up((size_t)R * L.nch2 * sizeof(float));
+  L.nacc = L.sums + align_up((size_t)R * L.nch2 * sizeof(float));
+  L.total = L.nacc + align_up((size_t)R * sizeof(int));
   return L;
 }
 
@@ -152,71 +152,6 @@ __device__ __forceinline__ void warp_merge_stat(float& m, float& z) {
   }
 }
 
-// The tail for problems too large for the shared-memory tables: one warp per
-// row, then one warp per request.
-__device__ __noinline__ void tail_warps(const float* __restrict__ logits, int T, int V, int R, int k,
-                                        float s, int nchunks, const int32_t* __restrict__ draft_tokens,
-                                        const float* __restrict__ draft_probs,
-                                        const float* __restrict__ uniforms,
-                                        const int32_t* __restrict__ kv_lens_in,
-                                        int32_t* __restrict__ accepted,
-                                        int32_t* __restrict__ kv_lens_out,
-                                        const float2* __restrict__ stats, float2* __restrict__ rowstat,
-                                        Decision* __restrict__ decisions) {
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  for (int tt = tid >> 5; tt < T; tt += kWarps) {
-    float mm = -INFINITY, zz = 0.f;
-    const float2* sr = stats + (long long)tt * nchunks;
-    for (int j = lane; j < nchunks; j += 32) {
-      const float2 v = __ldcg(sr + j);
-      merge_stat(mm, zz, v.x, v.y);
-    }
-    warp_merge_stat(mm, zz);
-    if (lane == 0) rowstat[tt] = make_float2(mm, 1.0f / zz);
-  }
-  __syncthreads();
-  // ---- acceptance: one warp per request, lane j tests draft j
-  for (int r = tid >> 5; r < R; r += kWarps) {
-    const int base = r * (k + 1);
-    int n = k;
-    for (int j0 = 0; j0 < k; j0 += 32) {
-      const int j = j0 + lane;
-      bool reject = false;
-      if (j < k) {
-        const int d = __ldg(draft_tokens + (long long)r * k + j);
-        // a draft id outside the vocabulary is rejected (never read)
-        if (d < 0 || d >= V) {
-          reject = true;
-        } else {
-          const float2 st = rowstat[base + j];
-          const float p =
-              fast_exp2(fmaf(__ldg(logits + (long long)(base + j) * V + d), s, -st.x)) * st.y;
-          const float q = __ldg(draft_probs + ((long long)r * k + j) * V + d);
-          const float u = __ldg(uniforms + (long long)r * (k + 1) + j);
-          reject = !(u * q < p);
-        }
-      }
-      const unsigned msk = __ballot_sync(0xFFFFFFFFu, reject);
-      if (msk) { n = j0 + __ffs(msk) - 1; break; }
-    }
-    if (lane == 0) {
-      Decision dcs;
-      dcs.n = n;
-      dcs.row = base + n;
-      dcs.mode = n < k ? 1 : 0;
-      dcs.pad = 0;
-      const float2 st = rowstat[base + n];
-      dcs.m2 = st.x;
-      dcs.inv_z = st.y;
-      dcs.pad2[0] = dcs.pad2[1] = 0.f;
-      decisions[r] = dcs;
-      accepted[r] = n;
-      kv_lens_out[r] = kv_lens_in[r] - (k - n);
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // kernel 1: row statistics, then the acceptance decisions
 // ---------------------------------------------------------------------------
@@ -227,12 +162,11 @@ __global__ void __launch_bounds__(kThreads)
                          const float* __restrict__ draft_probs, const float* __restrict__ uniforms,
                          const int32_t* __restrict__ kv_lens_in, int32_t* __restrict__ accepted,
                          int32_t* __restrict__ kv_lens_out, unsigned int* __restrict__ ticket,
-                         float2* __restrict__ stats, float2* __restrict__ rowstat,
-                         Decision* __restrict__ decisions) {
+                         float2* __restrict__ stats, float2* rowstat,
+                         Decision* __restrict__ decisions, int* n_acc) {
+  // shared memory stays under 1 KB (the attention kernel leaves ~1.8 KB of
+  // an SM's shared memory to kernels that run beside it)
   __shared__ float s_m[kWarps], s_z[kWarps];
-  __shared__ float2 s_stat[kTailStats];
-  __shared__ float2 s_row[kTailRows];
-  __shared__ int s_n[kTailRows];
   __shared__ bool s_last;
   const int tid = threadIdx.x;
   const int t = (int)(blockIdx.x / nchunks);
@@ -298,58 +232,61 @@ __global__ void __launch_bounds__(kThreads)
   if (!s_last) return;
 
   // ---- last CTA: row statistics, then the acceptance tests.  The loads of
-  // each phase are issued at once (block-strided) and meet in shared memory,
-  // so the tail costs a few memory round trips, not one per row.
+  // each phase are issued at once (block-strided) and the results meet in
+  // workspace slots (L2 atomics), so the tail costs a few memory round trips.
+  // Global writes of this block are visible to its threads after
+  // __syncthreads; the reads go to L2 (.cg).
   __threadfence();
-  const long long nstat = (long long)T * nchunks;
-  if (nstat <= kTailStats && T <= kTailRows && R <= kTailRows) {
-    for (long long f = tid; f < nstat; f += kThreads) s_stat[f] = __ldcg(stats + f);
-    for (int r = tid; r < R; r += kThreads) s_n[r] = k;
-    __syncthreads();
-    for (int tt = tid; tt < T; tt += kThreads) {
-      float mm = -INFINITY, zz = 0.f;
-      for (int j = 0; j < nchunks; ++j) {
-        const float2 v = s_stat[tt * nchunks + j];
-        merge_stat(mm, zz, v.x, v.y);
-      }
-      s_row[tt] = make_float2(mm, 1.0f / zz);
+  for (int r = tid; r < R; r += kThreads) n_acc[r] = k;
+  for (int tt = tid; tt < T; tt += kThreads) {
+    float mm = -INFINITY, zz = 0.f;
+    const float2* sr = stats + (long long)tt * nchunks;
+    int j = 0;
+    for (; j + 4 <= nchunks; j += 4) {
+      float2 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcg(sr + j + u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) merge_stat(mm, zz, v[u].x, v[u].y);
     }
-    __syncthreads();
-    const long long nd = (long long)R * k;
-    for (long long f = tid; f < nd; f += kThreads) {
-      const int r = (int)(f / k), j = (int)(f % k);
-      const int t = r * (k + 1) + j;
-      const int d = __ldg(draft_tokens + f);
-      bool reject = true;  // a draft id outside the vocabulary is rejected (never read)
-      if (d >= 0 && d < V) {
-        const float2 st = s_row[t];
-        const float p = fast_exp2(fmaf(__ldg(logits + (long long)t * V + d), s, -st.x)) * st.y;
-        const float q = __ldg(draft_probs + f * V + d);
-        const float u = __ldg(uniforms + (long long)r * (k + 1) + j);
-        reject = !(u * q < p);
-      }
-      if (reject) atomicMin(&s_n[r], j);
+    for (; j < nchunks; ++j) {
+      const float2 v = __ldcg(sr + j);
+      merge_stat(mm, zz, v.x, v.y);
     }
-    __syncthreads();
-    for (int r = tid; r < R; r += kThreads) {
-      const int n = s_n[r];
-      const int base = r * (k + 1);
-      Decision dcs;
-      dcs.n = n;
-      dcs.row = base + n;
-      dcs.mode = n < k ? 1 : 0;
-      dcs.pad = 0;
-      const float2 st = s_row[base + n];
-      dcs.m2 = st.x;
-      dcs.inv_z = st.y;
-      dcs.pad2[0] = dcs.pad2[1] = 0.f;
-      decisions[r] = dcs;
-      accepted[r] = n;
-      kv_lens_out[r] = kv_lens_in[r] - (k - n);
+    rowstat[tt] = make_float2(mm, 1.0f / zz);
+  }
+  __syncthreads();
+  const long long nd = (long long)R * k;
+  for (long long f = tid; f < nd; f += kThreads) {
+    const int r = (int)(f / k), j = (int)(f % k);
+    const int t = r * (k + 1) + j;
+    const int d = __ldg(draft_tokens + f);
+    bool reject = true;  // a draft id outside the vocabulary is rejected (never read)
+    if (d >= 0 && d < V) {
+      const float2 st = __ldcg(rowstat + t);
+      const float p = fast_exp2(fmaf(__ldg(logits + (long long)t * V + d), s, -st.x)) * st.y;
+      const float q = __ldg(draft_probs + f * V + d);
+      const float u = __ldg(uniforms + (long long)r * (k + 1) + j);
+      reject = !(u * q < p);
     }
-  } else {
-    tail_warps(logits, T, V, R, k, s, nchunks, draft_tokens, draft_probs, uniforms, kv_lens_in,
-               accepted, kv_lens_out, stats, rowstat, decisions);
+    if (reject) atomicMin(n_acc + r, j);
+  }
+  __syncthreads();
+  for (int r = tid; r < R; r += kThreads) {
+    const int n = __ldcg(n_acc + r);
+    const int base = r * (k + 1);
+    Decision dcs;
+    dcs.n = n;
+    dcs.row = base + n;
+    dcs.mode = n < k ? 1 : 0;
+    dcs.pad = 0;
+    const float2 st = __ldcg(rowstat + base + n);
+    dcs.m2 = st.x;
+    dcs.inv_z = st.y;
+    dcs.pad2[0] = dcs.pad2[1] = 0.f;
+    decisions[r] = dcs;
+    accepted[r] = n;
+    kv_lens_out[r] = kv_lens_in[r] - (k - n);
   }
   if (tid == 0) *ticket = 0u;
 }
@@ -897,10 +834,11 @@ extern "C" sv_status spec_verify_sampled(const float* logits, int R, int k, int 
   auto* rowstat = reinterpret_cast<float2*>(ws + L.rowstat);
   auto* dec = reinterpret_cast<sv::Decision*>(ws + L.decisions);
   auto* sums = reinterpret_cast<float*>(ws + L.sums);
+  auto* nacc = reinterpret_cast<int*>(ws + L.nacc);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   sv::sampled_stats_kernel<<<(unsigned)blocks1, sv::kThreads, 0, st>>>(
       logits, (int)T, V, R, k, s, L.chunk1, L.nch1, vec4, draft_tokens, draft_probs, uniforms,
-      kv_lens_in, accepted, kv_lens_out, ticket1, stats, rowstat, dec);
+      kv_lens_in, accepted, kv_lens_out, ticket1, stats, rowstat, dec, nacc);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_LAUNCH;
 
   cudaLaunchConfig_t cfg = {};

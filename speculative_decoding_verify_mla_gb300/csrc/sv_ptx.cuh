@@ -95,6 +95,11 @@ __device__ __forceinline__ float ld_dep_f32(const float* p) {
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ int ld_dep_s32(const int* p) {
+  int v;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ float4 ld_dep_f4_stream(const float4* p) {
   float4 v;
   asm volatile("ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%4];"

@@ -54,6 +54,14 @@ class VerifyStep:
         return self.out, self.lse, self.argmax, self.accepted, self.next_tokens, self.kv_lens_out
 
     @property
+    def attention_launches(self) -> int:
+        """Kernels one mla_verify_decode call enqueues: the balanced plan adds a
+        plan kernel and the merge; uniform splits add the merge when S > 1."""
+        if self.num_splits == B.SV_SPLITS_BALANCED:
+            return 3
+        return 1 + (1 if self.num_splits > 1 else 0)
+
+    @property
     def launches_per_step(self) -> int:
-        """Kernels one step enqueues: attention (+ combine when split) + greedy."""
-        return 1 + (1 if self.num_splits > 1 else 0) + 1
+        """Kernels one step enqueues: the attention call's kernels + greedy."""
+        return self.attention_launches + 1

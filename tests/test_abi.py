@@ -133,3 +133,19 @@ def test_sampled_host_checks(lib):
     assert f(*bad) == 4
     bad = list(args); bad[12] = 4096 + 16
     assert f(*bad) == 3                     # workspace 256-byte aligned
+
+
+def test_balanced_plan_host_checks(lib):
+    assert _attn_call(lib, splits=-2) == 2                       # only -1 is a valid negative
+    assert _attn_call(lib, splits=-1) == 4                       # the plan needs a workspace
+    assert _attn_call(lib, splits=-1, maxp=70000) == 2           # piece bounds are 16-bit
+    from speculative_decoding_verify_mla_gb300 import SV_SPLITS_BALANCED, attention_workspace_bytes
+    assert SV_SPLITS_BALANCED == -1
+    assert attention_workspace_bytes(128, 64, -1) > 128 * 64 * 2052
+
+
+def test_auto_split_choice(lib):
+    from speculative_decoding_verify_mla_gb300 import num_splits_for
+    assert num_splits_for(1, 8, 64, 24) >= 1       # one request: uniform splits
+    assert num_splits_for(16, 8, 64, 512) == -1    # long contexts, one wave: balanced plan
+    assert num_splits_for(32, 5, 64, 24) >= 1      # short contexts: uniform splits

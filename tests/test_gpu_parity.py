@@ -374,3 +374,43 @@ def test_kv_append_bad_data(sv):
     ref_pool = oracle.ref_kv_append(before.view(torch.int16).cpu().numpy().view(np.uint16),
                                     inp["block_table"], bad, kv_new, k1)
     assert np.array_equal(d["kv"].view(torch.int16).cpu().numpy().view(np.uint16), ref_pool)
+
+
+# ----------------------------------------------------------------- balanced split plan
+@pytest.mark.parametrize("lens", [(70, 4000, 333, 64, 1500), (5000,), (64, 65, 63, 4, 700, 2000, 129)])
+def test_balanced_plan_matches_oracle(sv, lens):
+    """Requests of very different lengths cut into pieces by the device-side plan."""
+    cfg = small_config("c2", R=len(lens), k=3, H=32, kv_lens=lens, kv_len_range=None, shuffled=True,
+                       vocab=64)
+    inp = make_inputs(cfg, seed=21)
+    ref_o, ref_l = oracle_attention(inp)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse = run_attention(sv, inp, num_splits=sv.SV_SPLITS_BALANCED, status=status)
+    assert int(status.item()) == 0
+    check_attention(out, lse, ref_o, ref_l, label=f"balanced {lens}")
+
+
+def test_balanced_plan_zero_bounds_and_nan_slack(sv):
+    inp = make_inputs(_mid_config(kv_lens=(70, 2000, 333)), seed=22)
+    k1 = inp["k"] + 1
+    bounds = inp["kv_bounds"].copy()
+    bounds[0] = 0
+    bounds[k1:2 * k1] = 0  # the long request fully masked: one empty piece
+    kv = inp["kv_bits"].copy()
+    bt = inp["block_table"]
+    for r in range(inp["R"]):
+        L = int(inp["kv_lens_in"][r])
+        last = int(bt[r, (L - 1) // 64])
+        kv[last, L % 64 if L % 64 else 64:] = 0x7FC0
+    ref_o, ref_l = oracle_attention(inp, bounds=bounds, kv_bits=kv)
+    out, lse = run_attention(sv, inp, num_splits=sv.SV_SPLITS_BALANCED, bounds=bounds, kv_bits=kv)
+    check_attention(out, lse, ref_o, ref_l, label="balanced zero bounds + nan slack")
+
+
+@pytest.mark.parametrize("H,k,lens", [(96, 1, (300, 129, 3000)), (1, 0, (65, 1, 640)), (8, 19, (500, 64))])
+def test_balanced_plan_head_shapes(sv, H, k, lens):
+    cfg = small_config("c0", R=len(lens), k=k, H=H, kv_lens=lens, shuffled=True, vocab=64)
+    inp = make_inputs(cfg, seed=23)
+    ref_o, ref_l = oracle_attention(inp)
+    out, lse = run_attention(sv, inp, num_splits=sv.SV_SPLITS_BALANCED)
+    check_attention(out, lse, ref_o, ref_l, label=f"balanced H={H} k={k}")
