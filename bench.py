@@ -54,6 +54,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(times_ms, device, world):
+    """Mean of this rank's per-step times, then the maximum over all ranks
+    (all_reduce MAX over the default process group when world > 1)."""
+    m = statistics.mean(times_ms)
+    if world > 1:
+        import torch
+        t = torch.tensor([m], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        m = float(t.item())
+    return m
+
+
+def replica_throughput(step_ms, world):
+    """Steps per second of the whole job: every rank runs its own replica."""
+    return world * 1000.0 / step_ms
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -347,12 +364,7 @@ def main():
 
     # max over ranks
     def agg(xs):
-        m = statistics.mean(xs)
-        if world > 1:
-            t = torch.tensor([m], dtype=torch.float64, device=device)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            m = float(t.item())
-        return m
+        return max_over_ranks(xs, device, world)
 
     step_mean, attn_mean, greedy_mean, e2e_mean = (agg(step_ms), agg(attn_ms), agg(greedy_ms), agg(e2e_ms))
     append_mean = agg(append_ms)
@@ -410,7 +422,7 @@ def main():
         "kv_append_gbps": T * 2 * 1024 / (append_mean * 1e-3) / 1e9,
         "sampled_verify_us": sampled_mean * 1000.0,
         "sampled_verify_gbps": (T + 2 * R) * V * 4 / (sampled_mean * 1e-3) / 1e9,
-        "steps_per_s_all_gpus": world * 1000.0 / step_mean,
+        "steps_per_s_all_gpus": replica_throughput(step_mean, world),
         "roofline": roof,
         "cpu_baseline": base,
         "e2e": {"value": e2e_mean * 1000.0, "unit": "us", "h2d_bytes_per_step": h2d,
