@@ -24,6 +24,16 @@ What it computes, written as the plain definitions (no blocking, no fusion):
   [T, H, 512] elementwise sigmoid gate applied to the normalised output).
   PARITY UNPINNED for the gate's shape and placement: the pages do not fix
   them; the pins below only fix sigmoid(g) * o for the reading taken.
+* Head-wise gate.  A gate of shape [T, H] (one value per token and head)
+  scales the whole 512-wide latent row: out = sigmoid(gate[t, h]) * o[t, h]
+  ("next" variant of the Kimi K3 helix configuration in "TensorRT-LLM PR
+  #18166", which runs H = 96; a head-wise gate is the form that commutes
+  with the per-head value up-projection W_UV).
+* Value up-projection (``ref_wuv_project``): the absorbed latent output of
+  head h is mapped to the head's value space by W_UV[h] (v_dim x 512):
+  v[t, h] = W_UV[h] @ out[t, h] ("LSE combine + W_UV" after the context-
+  parallel merge, vLLM page "kimi_k3/nvidia/specialized_decode/drafter/
+  model"; absorbed MLA keeps W_UV out of the attention).
 * Split-KV partials and their merge (``ref_attention_partials``,
   ``ref_lse_combine``): each KV range gives (o_s, lse_s) by the same formula;
   lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s, and an all
@@ -95,9 +105,10 @@ def _softmax_stats(s: np.ndarray, rows: np.ndarray):
 def ref_verify_attention(q, kv_pages, block_table, kv_bounds, gate, q_per_req, softmax_scale):
     """Gated, absorbed NoPE MLA decode attention with per-token bounds.
 
-    q, gate: [T, H, D] (float64 or bf16 bits); kv_pages: [P, page, D];
-    block_table: [R, max_pages]; kv_bounds: [T].  Returns (out [T, H, D],
-    lse [T, H]) in float64; out is gated, lse is of the ungated scaled scores.
+    q: [T, H, D], gate: [T, H, D] (elementwise) or [T, H] (head-wise), float64
+    or bf16 bits; kv_pages: [P, page, D]; block_table: [R, max_pages];
+    kv_bounds: [T].  Returns (out [T, H, D], lse [T, H]) in float64; out is
+    gated, lse is of the ungated scaled scores.
     """
     q = _as_f64(q)
     g = _as_f64(gate)
@@ -114,8 +125,29 @@ def ref_verify_attention(q, kv_pages, block_table, kv_bounds, gate, q_per_req, s
             rows = rows_all[:int(kv_bounds[t])]
             s = softmax_scale * (q[t] @ rows.T)
             lse[t], o = _softmax_stats(s, rows)
-            out[t] = sigmoid(g[t]) * o
+            out[t] = gate_factor(g[t]) * o
     return out, lse
+
+
+def gate_factor(g_t: np.ndarray) -> np.ndarray:
+    """sigmoid of one token's gate, shaped to multiply its [H, D] output: a
+    head-wise gate [H] becomes a column [H, 1]."""
+    sg = sigmoid(g_t)
+    return sg[:, None] if sg.ndim == 1 else sg
+
+
+def ref_wuv_project(out_latent, w_uv) -> np.ndarray:
+    """Per-head value up-projection v[t, h, :] = W_UV[h] @ out[t, h, :].
+
+    out_latent [T, H, D] (float64 or bf16 bits), w_uv [H, v_dim, D] (float64 or
+    bf16 bits).  Returns [T, H, v_dim] float64."""
+    x = _as_f64(out_latent)
+    w = _as_f64(w_uv)
+    T, H, D = x.shape
+    v = np.zeros((T, H, w.shape[1]))
+    for h in range(H):
+        v[:, h, :] = x[:, h, :] @ w[h].T
+    return v
 
 
 def ref_attention_partials(q, kv_pages, block_table, kv_bounds, q_per_req, softmax_scale, edges):
@@ -159,7 +191,8 @@ def ref_lse_combine(part_o, part_lse, gate=None):
     w = np.where(empty[None], 0.0, w_raw / np.where(empty, 1.0, z)[None])
     o = (w[..., None] * part_o).sum(axis=0)
     if gate is not None:
-        o = sigmoid(_as_f64(gate)) * o
+        g = sigmoid(_as_f64(gate))
+        o = (g[..., None] if g.ndim == o.ndim - 1 else g) * o
     return o, lse
 
 

@@ -830,13 +830,14 @@ bool device_setup(int* sm_count) {
 }
 
 // Splits: enough (request, row tile, split, latent half) CTAs to fill the SMs
-// once, each split keeping at least 4 KV tiles.
+// once, each split keeping at least 2 KV tiles (on the C = 1 verify batch,
+// 24 tiles: 12 splits 22.7 us, 8: 22.9, 6: 24.7, 19: 24.9 measured).
 int auto_splits(int R, int q_per_req, int H, int max_pages, int sm_count) {
   const long long n_mt = ((long long)H * q_per_req + kMTile - 1) / kMTile;
   const long long ctas = 2ll * R * n_mt;
   if (ctas <= 0) return 1;
   long long s = (long long)sm_count / ctas;
-  const long long by_len = max_pages / 4;
+  const long long by_len = max_pages / 2;
   if (s > by_len) s = by_len;
   if (s > SV_MAX_SPLITS) s = SV_MAX_SPLITS;
   if (s < 1) s = 1;

@@ -499,3 +499,69 @@ def pin_sampled_greedy_limit(orc):
 
 SAMPLED_PINS = [pin_sampled_distribution, pin_sampled_hand_cases, pin_sampled_closed_forms,
                 pin_sampled_greedy_limit]
+
+
+# --------------------------------------------------------------------------
+# head-wise gate and the W_UV value up-projection
+# --------------------------------------------------------------------------
+def pin_headwise_gate(orc):
+    """A [T, H] gate scales whole latent rows: brute force on sampled rows,
+    the gate-0 closed form (half the ungated output) and equality with the
+    same values broadcast over the 512 columns."""
+    inp = make_inputs("c0", seed=0)
+    k1 = inp["k"] + 1
+    g_head = inp["gate_bits"][:, :, 0].copy()  # bf16 bits [T, H]
+    out_hw, lse_hw = orc.ref_verify_attention(inp["q_bits"], inp["kv_bits"], inp["block_table"],
+                                              inp["kv_bounds"], g_head, k1, inp["softmax_scale"])
+    for t, h in ((0, 0), (5, 3), (7, 7)):
+        b = dict(inp)
+        b["gate_bits"] = np.repeat(g_head[:, :, None], inp["gate_bits"].shape[2], axis=2)
+        lse_b, out_b = brute_row(b, t, h)
+        assert abs(lse_hw[t, h] - lse_b) < 1e-9
+        assert np.allclose(out_hw[t, h], out_b, rtol=1e-9, atol=1e-12)
+    zero = np.zeros_like(g_head)
+    out0, _ = orc.ref_verify_attention(inp["q_bits"], inp["kv_bits"], inp["block_table"], inp["kv_bounds"],
+                                       zero, k1, inp["softmax_scale"])
+    big = np.full(inp["gate_bits"].shape, 60.0)
+    out_ungated, _ = orc.ref_verify_attention(inp["q_bits"], inp["kv_bits"], inp["block_table"],
+                                              inp["kv_bounds"], big, k1, inp["softmax_scale"])
+    assert np.allclose(out0, 0.5 * out_ungated, rtol=1e-12, atol=1e-14)
+    # the merge applies the head-wise gate the same way
+    po, pl = orc.ref_attention_partials(inp["q_bits"], inp["kv_bits"], inp["block_table"], inp["kv_bounds"], k1,
+                                        inp["softmax_scale"], [[0, 40, 100], [0, 30, 100]])
+    om, lm = orc.ref_lse_combine(po, pl, g_head)
+    assert np.allclose(om, out_hw, rtol=1e-9, atol=1e-12)
+    fin = np.isfinite(lse_hw)
+    assert np.array_equal(np.isfinite(lm), fin) and np.allclose(lm[fin], lse_hw[fin], rtol=0, atol=1e-9)
+
+
+def pin_wuv_projection(orc):
+    """v[t, h] = W_UV[h] @ out[t, h]: scalar brute force (exactly rounded
+    sums), the identity projection, and commuting with a head-wise gate."""
+    rng = np.random.default_rng(31)
+    T, H, D, V = 3, 4, 512, 16
+    x = rng.standard_normal((T, H, D))
+    w = rng.standard_normal((H, V, D))
+    v = orc.ref_wuv_project(x, w)
+    assert v.shape == (T, H, V)
+    for t in range(T):
+        for h in range(H):
+            for j in (0, 7, V - 1):
+                ref = math.fsum(float(w[h, j, d]) * float(x[t, h, d]) for d in range(D))
+                assert abs(v[t, h, j] - ref) < 1e-10
+    eye = np.broadcast_to(np.eye(D), (H, D, D))
+    assert np.allclose(orc.ref_wuv_project(x, eye), x, rtol=0, atol=1e-12)
+    # bf16 bit inputs widen exactly
+    xb = f32_to_bf16_bits(x.astype(np.float32))
+    wb = f32_to_bf16_bits(w.astype(np.float32))
+    vb = orc.ref_wuv_project(xb, wb)
+    xf = np.array([[[bf16_to_float(a) for a in row] for row in m] for m in xb[:1, :1]])
+    wf = np.array([[bf16_to_float(a) for a in row] for row in wb[0, :2]])
+    assert abs(vb[0, 0, 1] - math.fsum(float(p) * float(q) for p, q in zip(wf[1], xf[0, 0]))) < 1e-9
+    # a head-wise gate commutes with the projection
+    g = rng.standard_normal((T, H))
+    sg = 1.0 / (1.0 + np.exp(-g))
+    assert np.allclose(orc.ref_wuv_project(sg[..., None] * x, w), sg[..., None] * v, rtol=1e-12, atol=1e-12)
+
+
+ALL_PINS += [pin_headwise_gate, pin_wuv_projection]

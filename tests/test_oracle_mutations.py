@@ -132,7 +132,29 @@ def _mut_nan_identity(m):
     m._softmax_stats = f
 
 
+def _mut_wuv_wrong_head(m):
+    orig = m.ref_wuv_project
+    m.ref_wuv_project = lambda x, w: orig(x, np.roll(m._as_f64(w), 1, axis=0))
+
+
+def _mut_headwise_gate_ignored(m):
+    orig = m.gate_factor
+    m.gate_factor = lambda g: np.ones((len(g), 1)) if np.asarray(g).ndim == 1 else orig(g)
+
+
+def _mut_wuv_transposed_input(m):
+    def f(x, w):
+        x = m._as_f64(x)
+        w = m._as_f64(w)
+        v = np.zeros((x.shape[0], x.shape[1], w.shape[1]))
+        for h in range(x.shape[1]):
+            v[:, h, :] = x[:, h, ::-1] @ w[h].T  # latent columns reversed
+        return v
+    m.ref_wuv_project = f
+
+
 MUTATIONS = [
+    _mut_wuv_wrong_head, _mut_headwise_gate_ignored, _mut_wuv_transposed_input,
     _mut_bound_off_by_one, _mut_no_scale, _mut_gate_sign, _mut_token_mapping, _mut_lse_log2,
     _mut_argmax_last, _mut_draft_position, _mut_trim, _mut_unnormalised_merge, _mut_nan_identity,
 ]
