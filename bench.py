@@ -334,6 +334,14 @@ def main():
                                                       temperature=sinp["temperature"], workspace=s_ws,
                                                       accepted=s_out[0], next_tokens=s_out[1],
                                                       kv_lens_out=s_out[2]), args.steps)
+    # per-head W_UV value up-projection of the attention output (v_dim 128,
+    # seeded bf16 weights), the step after the merge
+    from workloads import f32_to_bf16_bits
+    w_np = f32_to_bf16_bits(np.random.default_rng(rank + 7).standard_normal((H, 128, 512), dtype=np.float32)
+                            / np.float32(16.0))
+    w_uv = torch.from_numpy(w_np.view(np.int16)).view(torch.bfloat16).to(device)
+    out_v = torch.empty((T, H, 128), dtype=torch.bfloat16, device=device)
+    wuv_ms = timed(lambda: sv.mla_wuv_project(step.out, w_uv, out_v=out_v), args.steps)
     barrier()
     clocks = sampler.stop() if not args.no_clocks else None
 
@@ -369,6 +377,7 @@ def main():
     step_mean, attn_mean, greedy_mean, e2e_mean = (agg(step_ms), agg(attn_ms), agg(greedy_ms), agg(e2e_ms))
     append_mean = agg(append_ms)
     sampled_mean = agg(sampled_ms)
+    wuv_mean = agg(wuv_ms)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -422,6 +431,8 @@ def main():
         "kv_append_gbps": T * 2 * 1024 / (append_mean * 1e-3) / 1e9,
         "sampled_verify_us": sampled_mean * 1000.0,
         "sampled_verify_gbps": (T + 2 * R) * V * 4 / (sampled_mean * 1e-3) / 1e9,
+        "wuv_project_us": wuv_mean * 1000.0,
+        "wuv_project_tflops": 2.0 * T * H * 128 * 512 / (wuv_mean * 1e-3) / 1e12,
         "steps_per_s_all_gpus": replica_throughput(step_mean, world),
         "roofline": roof,
         "cpu_baseline": base,
@@ -429,7 +440,7 @@ def main():
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * step.launches_per_step,
         "gpu_launches_all_timed_loops": args.steps * (2 * step.launches_per_step + step.attention_launches
-                                                       + 1 + 1 + 2),
+                                                       + 1 + 1 + 2 + 1),
         "clocks": clocks,
         "status_word": int(step.status.item()),
     }

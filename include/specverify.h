@@ -11,6 +11,8 @@
  *                       latent rows, bounded per token, split over KV, with
  *                       the LSE merge and the sigmoid gate fused in.
  *   mla_lse_combine     the LSE merge + gate of split partials on its own.
+ *   mla_verify_decode_gated  the same with a head-wise ([T][H]) gate.
+ *   mla_wuv_project     the per-head W_UV value up-projection after the merge.
  *   mla_kv_append       the verify tokens' latent rows into the paged cache.
  *   spec_verify_sampled rejection-sampling verification (probabilistic drafts).
  *   spec_verify_greedy  target argmax, accepted draft prefix, next token and
@@ -147,6 +149,46 @@ sv_status mla_verify_decode(const void* q_latent, const void* kv_pages, int num_
                             int H, float softmax_scale, int num_splits, void* workspace,
                             size_t workspace_bytes, void* out, float* lse, int32_t* status,
                             sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * mla_verify_decode_gated
+ *
+ * mla_verify_decode with a choice of gate shape (the head-wise form is the
+ * "next" variant for the H = 96 Kimi K3 configuration of "TensorRT-LLM PR
+ * #18166"; only a gate that is constant over a head's latent row commutes
+ * with the later per-head W_UV projection):
+ *   gate_dim == 512: gate bf16 [T][H][512], out = sigmoid(gate) * o
+ *                    elementwise (exactly mla_verify_decode);
+ *   gate_dim == 1:   gate bf16 [T][H], out[t][h][:] = sigmoid(gate[t][h]) * o.
+ * Any other gate_dim returns SV_ERR_UNSUPPORTED.  All other arguments,
+ * layouts and errors as mla_verify_decode; gate must be 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+sv_status mla_verify_decode_gated(const void* q_latent, const void* kv_pages, int num_pages,
+                                  int page_size, const int32_t* block_table, int R,
+                                  int q_per_req, int max_pages_per_req, const int32_t* kv_bounds,
+                                  const void* gate, int gate_dim, int H, float softmax_scale,
+                                  int num_splits, void* workspace, size_t workspace_bytes,
+                                  void* out, float* lse, int32_t* status, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * mla_wuv_project
+ *
+ * Per-head value up-projection of the absorbed attention output, the
+ * "LSE combine + W_UV" step after the merge (vLLM page
+ * "kimi_k3/nvidia/specialized_decode/drafter/model"):
+ *     out_v[t][h][j] = sum_d w_uv[h][j][d] * x[t][h][d]     (fp32 accumulate)
+ *
+ *   x       bf16 [T][H][512] (e.g. the out of mla_verify_decode), 16-byte
+ *           aligned.
+ *   w_uv    bf16 [H][v_dim][512], 16-byte aligned.
+ *   v_dim   a multiple of 32 in [32, 256] (else SV_ERR_UNSUPPORTED).
+ *   out_v   bf16 [T][H][v_dim] (round to nearest even), 16-byte aligned.
+ *   status  device int32 ORed with SV_DEV_TIMEOUT if a bounded wait gives
+ *           up; may be NULL.
+ * One tcgen05 GEMM per (head, 128-token tile) on `stream`.
+ * ---------------------------------------------------------------------- */
+sv_status mla_wuv_project(const void* x, const void* w_uv, int T, int H, int v_dim, void* out_v,
+                          int32_t* status, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * mla_kv_append

@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     mla_kv_append,
     mla_lse_combine,
     mla_verify_decode,
+    mla_wuv_project,
     num_splits_for,
     sampled_workspace,
     sampled_workspace_bytes,

@@ -40,6 +40,8 @@ EXPORTED_SYMBOLS = (
     "mla_kv_append",
     "sv_sampled_workspace_bytes",
     "spec_verify_sampled",
+    "mla_verify_decode_gated",
+    "mla_wuv_project",
 )
 
 _lib = None
@@ -93,6 +95,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             _c_void_p, _c_int, _c_int, _c_int, _c_float, _c_void_p, _c_void_p, _c_void_p,
             _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_size, _c_void_p]
         lib.spec_verify_sampled.restype = _c_int
+        lib.mla_verify_decode_gated.argtypes = [
+            _c_void_p, _c_void_p, _c_int, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_void_p,
+            _c_void_p, _c_int, _c_int, _c_float, _c_int, _c_void_p, _c_size, _c_void_p, _c_void_p,
+            _c_void_p, _c_void_p]
+        lib.mla_verify_decode_gated.restype = _c_int
+        lib.mla_wuv_project.argtypes = [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_void_p,
+                                        _c_void_p, _c_void_p]
+        lib.mla_wuv_project.restype = _c_int
         _lib = lib
         return lib
 
@@ -151,7 +161,9 @@ def mla_verify_decode(q_latent: torch.Tensor, kv_pages: torch.Tensor, block_tabl
         _check(t.device == dev, f"{name} must be on {dev}")
         _check(t.is_contiguous(), f"{name} must be contiguous")
     _check(kv_pages.dim() == 3 and kv_pages.shape[2] == SV_LATENT_DIM, "kv_pages must be [P, page, 512]")
-    _check(tuple(gate.shape) == (T, H, SV_LATENT_DIM), "gate must match q_latent")
+    _check(tuple(gate.shape) in ((T, H, SV_LATENT_DIM), (T, H)),
+           "gate must be [T, H, 512] (elementwise) or [T, H] (head-wise)")
+    gate_dim = SV_LATENT_DIM if gate.dim() == 3 else 1
     _check(block_table.dim() == 2, "block_table must be [R, max_pages]")
     R, max_pages = block_table.shape
     _check(T == R * q_per_req, "T must equal R * q_per_req")
@@ -166,9 +178,9 @@ def mla_verify_decode(q_latent: torch.Tensor, kv_pages: torch.Tensor, block_tabl
     if ws_bytes > 0 and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     ws_size = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    code = lib.mla_verify_decode(
+    code = lib.mla_verify_decode_gated(
         _ptr(q_latent), _ptr(kv_pages), int(kv_pages.shape[0]), int(kv_pages.shape[1]),
-        _ptr(block_table), R, q_per_req, max_pages, _ptr(kv_bounds), _ptr(gate), H,
+        _ptr(block_table), R, q_per_req, max_pages, _ptr(kv_bounds), _ptr(gate), gate_dim, H,
         float(softmax_scale), int(num_splits), _ptr(workspace), ws_size, _ptr(out), _ptr(lse),
         _ptr(status), _stream(dev))
     _check_status("mla_verify_decode", code)
@@ -317,3 +329,24 @@ def spec_verify_sampled(logits: torch.Tensor, draft_tokens: torch.Tensor, draft_
         workspace.numel() * workspace.element_size(), _stream(dev))
     _check_status("spec_verify_sampled", code)
     return tuple(outs)
+
+
+def mla_wuv_project(x: torch.Tensor, w_uv: torch.Tensor, out_v: torch.Tensor | None = None,
+                    status: torch.Tensor | None = None) -> torch.Tensor:
+    """Per-head value up-projection: x [T, H, 512] bf16, w_uv [H, v_dim, 512]
+    bf16 -> out_v [T, H, v_dim] bf16."""
+    lib = load_library()
+    _check(x.dim() == 3 and x.shape[2] == SV_LATENT_DIM, "x must be [T, H, 512]")
+    T, H, _ = x.shape
+    _check(w_uv.dim() == 3 and w_uv.shape[0] == H and w_uv.shape[2] == SV_LATENT_DIM,
+           "w_uv must be [H, v_dim, 512]")
+    v_dim = int(w_uv.shape[1])
+    dev = x.device
+    for name, t in (("x", x), ("w_uv", w_uv)):
+        _check(t.dtype == torch.bfloat16 and t.device == dev and t.is_contiguous(),
+               f"{name}: bf16, contiguous, on {dev}")
+    if out_v is None:
+        out_v = torch.empty((T, H, v_dim), dtype=torch.bfloat16, device=dev)
+    code = lib.mla_wuv_project(_ptr(x), _ptr(w_uv), T, H, v_dim, _ptr(out_v), _ptr(status), _stream(dev))
+    _check_status("mla_wuv_project", code)
+    return out_v

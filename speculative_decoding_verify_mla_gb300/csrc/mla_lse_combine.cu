@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     lse_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                        int S_uniform, long long rows, const __nv_bfloat16* __restrict__ gate,
                        __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out,
-                       const int* plan_splits, const int* plan_base, int Mq) {
+                       const int* plan_splits, const int* plan_base, int Mq, int gate_dim) {
   // one warp per half row (256 columns): lane owns columns 128j + 4 lane .. +3, j = 0, 1
   const int lane = threadIdx.x & 31;
   const long long hrow = (long long)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
@@ -41,10 +41,16 @@ __global__ void __launch_bounds__(kCombineThreads)
   const long long row = hrow >> 1;
   const int col0 = (int)(hrow & 1) * 256 + 4 * lane;
   // the gate does not depend on the attention kernel: fetch it first
-  uint2 graw[2];
+  // (elementwise [T][H][512], or one value per row when head-wise)
+  uint2 graw[2] = {make_uint2(0u, 0u), make_uint2(0u, 0u)};
+  float g_row = 0.f;
+  if (gate_dim == 1) {
+    g_row = fast_sigmoid(__bfloat162float(gate[row]));
+  } else {
 #pragma unroll
-  for (int j = 0; j < 2; ++j)
-    graw[j] = __ldg(reinterpret_cast<const uint2*>(gate + row * 512 + col0 + 128 * j));
+    for (int j = 0; j < 2; ++j)
+      graw[j] = __ldg(reinterpret_cast<const uint2*>(gate + row * 512 + col0 + 128 * j));
+  }
   // when launched behind the attention kernel (programmatic dependent
   // launch), wait here until its partials are complete and visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -108,8 +114,11 @@ __global__ void __launch_bounds__(kCombineThreads)
   for (int j = 0; j < 2; ++j) {
     const float2 ga = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw[j].x));
     const float2 gb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw[j].y));
-    const __nv_bfloat162 r0 = __floats2bfloat162_rn(fast_sigmoid(ga.x) * acc[j].x, fast_sigmoid(ga.y) * acc[j].y);
-    const __nv_bfloat162 r1 = __floats2bfloat162_rn(fast_sigmoid(gb.x) * acc[j].z, fast_sigmoid(gb.y) * acc[j].w);
+    const bool hw = (gate_dim == 1);
+    const __nv_bfloat162 r0 = __floats2bfloat162_rn((hw ? g_row : fast_sigmoid(ga.x)) * acc[j].x,
+                                                    (hw ? g_row : fast_sigmoid(ga.y)) * acc[j].y);
+    const __nv_bfloat162 r1 = __floats2bfloat162_rn((hw ? g_row : fast_sigmoid(gb.x)) * acc[j].z,
+                                                    (hw ? g_row : fast_sigmoid(gb.y)) * acc[j].w);
     uint2 packed;
     packed.x = *reinterpret_cast<const uint32_t*>(&r0);
     packed.y = *reinterpret_cast<const uint32_t*>(&r1);
@@ -123,7 +132,7 @@ __global__ void __launch_bounds__(kCombineThreads)
 // Internal launcher shared with mla_verify_decode (no argument checks).
 cudaError_t launch_lse_combine(const float* part_o, const float* part_lse, int S, long long rows,
                                const void* gate, void* out, float* lse, cudaStream_t stream,
-                               const int* plan_splits, const int* plan_base, int Mq) {
+                               const int* plan_splits, const int* plan_base, int Mq, int gate_dim) {
   if (rows == 0) return cudaSuccess;
   const long long blocks = (2 * rows + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
   // programmatic dependent launch: the grid may start while the previous
@@ -141,7 +150,7 @@ cudaError_t launch_lse_combine(const float* part_o, const float* part_lse, int S
   const cudaError_t e = cudaLaunchKernelEx(&cfg, lse_combine_kernel, part_o, part_lse, S, rows,
                                            static_cast<const __nv_bfloat16*>(gate),
                                            static_cast<__nv_bfloat16*>(out), lse, plan_splits,
-                                           plan_base, Mq);
+                                           plan_base, Mq, gate_dim);
   if (e != cudaSuccess) cudaGetLastError();
   return e;
 }
@@ -163,7 +172,7 @@ extern "C" sv_status mla_lse_combine(const float* part_o, const float* part_lse,
     return SV_ERR_ALIGN;
   return sv::launch_lse_combine(part_o, part_lse, S, rows, gate, out, lse,
                                 reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr,
-                                1) == cudaSuccess
+                                1, SV_LATENT_DIM) == cudaSuccess
              ? SV_OK
              : SV_ERR_LAUNCH;
 }

@@ -48,13 +48,14 @@
 #include <cstdint>
 #include <mutex>
 
+#include "sv_host.h"
 #include "sv_ptx.cuh"
 
 namespace sv {
 
 cudaError_t launch_lse_combine(const float* part_o, const float* part_lse, int S, long long rows,
                                const void* gate, void* out, float* lse, cudaStream_t stream,
-                               const int* plan_splits, const int* plan_base, int Mq);
+                               const int* plan_splits, const int* plan_base, int Mq, int gate_dim);
 
 namespace {
 
@@ -105,6 +106,7 @@ struct VerifyParams {
   const int4* units;
   const int* plan_header;
   long long part_w_stride;  // part_lse elements between consecutive slots
+  int gate_dim;             // 512: elementwise gate [T][H][512]; 1: head-wise gate [T][H]
 };
 
 __device__ __forceinline__ int load_bound(const VerifyParams& p, int tok) {
@@ -435,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(q_s + b * kQBoxBytes, &tmap_gate, gate_full, half * kDHalf + b * 64,
                     m_tile * kMTile, r);
     };
-    if (fused_gate && ntiles == 0 && leader) load_gate();
+    if (fused_gate && p.gate_dim != 1 && ntiles == 0 && leader) load_gate();
 
     float m_ref = -INFINITY;  // running max (log2 units) used for exponentiation
     float l_sum = 0.f;
@@ -444,7 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sb = it & 1;
       const uint32_t par = (it >> 1) & 1;
       if (!warp_wait(s_full(sb), par, abort_flag, p.status)) { ok = false; break; }
-      if (fused_gate && it == ntiles - 1 && leader) load_gate();  // last score GEMM is done
+      if (fused_gate && p.gate_dim != 1 && it == ntiles - 1 && leader)
+        load_gate();  // last score GEMM is done
       tc_fence_after();
       float x[64];
       {
@@ -522,7 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t row_off = (uint32_t)i * 128u;
     const uint32_t swz = (uint32_t)(i & 7);
     if (fused_gate) {
-      const bool gate_ok = warp_wait(gate_full, 0, abort_flag, p.status);
+      // head-wise gate: one sigmoid per row; elementwise: the staged gate tile
+      const bool row_gate = (p.gate_dim == 1);
+      const float g_row = (row_gate && valid) ? fast_sigmoid(__bfloat162float(p.gate[row_g])) : 0.f;
+      const bool gate_ok = !row_gate && warp_wait(gate_full, 0, abort_flag, p.status);
       const uint8_t* const gs = sptr + kOffQ;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
@@ -545,8 +551,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
-            const float o0 = __uint_as_float(v[8 * u + 2 * e]) * inv_l * fast_sigmoid(gf.x);
-            const float o1 = __uint_as_float(v[8 * u + 2 * e + 1]) * inv_l * fast_sigmoid(gf.y);
+            const float s0 = row_gate ? g_row : fast_sigmoid(gf.x);
+            const float s1 = row_gate ? g_row : fast_sigmoid(gf.y);
+            const float o0 = __uint_as_float(v[8 * u + 2 * e]) * inv_l * s0;
+            const float o1 = __uint_as_float(v[8 * u + 2 * e + 1]) * inv_l * s1;
             ow[e] = pack_bf16x2(o0, o1);
           }
           *reinterpret_cast<uint4*>(stage + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
@@ -774,39 +782,6 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// Tiled tensor map with 128-byte swizzle over a row-major tensor whose
-// innermost dimension is the 512-wide latent row.
-bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base,
-                int rank, const cuuint64_t* dims, const cuuint32_t* box) {
-  auto encode = get_encode_fn();
-  if (!encode) return false;
-  cuuint64_t strides[4];
-  cuuint64_t acc = (cuuint64_t)elem_bytes;
-  for (int d = 0; d + 1 < rank; ++d) {
-    acc *= dims[d];
-    strides[d] = acc;
-  }
-  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return encode(map, dtype, rank, const_cast<void*>(base), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices];
 bool g_attr_set[kMaxDevices];
@@ -912,16 +887,18 @@ extern "C" size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits) {
   return o_bytes + (size_t)num_splits * rows * sizeof(float);
 }
 
-extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_pages, int num_pages,
-                                       int page_size, const int32_t* block_table, int R,
-                                       int q_per_req, int max_pages_per_req,
-                                       const int32_t* kv_bounds, const void* gate, int H,
-                                       float softmax_scale, int num_splits, void* workspace,
-                                       size_t workspace_bytes, void* out, float* lse,
-                                       int32_t* status, sv_stream_t stream) {
+extern "C" sv_status mla_verify_decode_gated(const void* q_latent, const void* kv_pages,
+                                             int num_pages, int page_size,
+                                             const int32_t* block_table, int R, int q_per_req,
+                                             int max_pages_per_req, const int32_t* kv_bounds,
+                                             const void* gate, int gate_dim, int H,
+                                             float softmax_scale, int num_splits, void* workspace,
+                                             size_t workspace_bytes, void* out, float* lse,
+                                             int32_t* status, sv_stream_t stream) {
   using namespace sv;
   if (R < 0 || q_per_req < 1 || H < 1 || max_pages_per_req < 0 || num_pages < 0)
     return SV_ERR_SHAPE;
+  if (gate_dim != kD && gate_dim != 1) return SV_ERR_UNSUPPORTED;
   if (page_size != SV_PAGE_SIZE) return SV_ERR_UNSUPPORTED;
   if ((num_splits < 0 && num_splits != SV_SPLITS_BALANCED) || num_splits > SV_MAX_SPLITS)
     return SV_ERR_SHAPE;
@@ -977,7 +954,8 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
     const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (!encode_map(&tmap_kv, bf16, 2, kv_pages, 2, kv_dims, kv_box) ||
         !encode_map(&tmap_q, bf16, 2, q_latent, 3, row_dims, row_box) ||
-        !encode_map(&tmap_gate, bf16, 2, gate, 3, row_dims, row_box) ||
+        (gate_dim == kD ? !encode_map(&tmap_gate, bf16, 2, gate, 3, row_dims, row_box)
+                        : !encode_map(&tmap_gate, bf16, 2, q_latent, 3, row_dims, row_box)) ||
         !encode_map(&tmap_out, bf16, 2, out, 3, row_dims, row_box))
       return SV_ERR_ALIGN;
     if (balanced) {
@@ -1017,6 +995,7 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
   prm.units = nullptr;
   prm.plan_header = nullptr;
   prm.part_w_stride = T * H;
+  prm.gate_dim = gate_dim;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   if (!balanced) {
@@ -1026,7 +1005,7 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
                                                                    tmap_out, tmap_part, prm);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_LAUNCH;
     if (S > 1 && launch_lse_combine(part_o, part_lse, S, T * H, gate, out, lse, st, nullptr,
-                                    nullptr, 1) != cudaSuccess)
+                                    nullptr, 1, gate_dim) != cudaSuccess)
       return SV_ERR_LAUNCH;
     return SV_OK;
   }
@@ -1060,9 +1039,22 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
     return SV_ERR_LAUNCH;
   }
   if (launch_lse_combine(part_o, part_lse, 0, T * H, gate, out, lse, st, splits, pbase,
-                         (int)Mq_ll) != cudaSuccess)
+                         (int)Mq_ll, gate_dim) != cudaSuccess)
     return SV_ERR_LAUNCH;
   return SV_OK;
+}
+
+extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_pages, int num_pages,
+                                       int page_size, const int32_t* block_table, int R,
+                                       int q_per_req, int max_pages_per_req,
+                                       const int32_t* kv_bounds, const void* gate, int H,
+                                       float softmax_scale, int num_splits, void* workspace,
+                                       size_t workspace_bytes, void* out, float* lse,
+                                       int32_t* status, sv_stream_t stream) {
+  return mla_verify_decode_gated(q_latent, kv_pages, num_pages, page_size, block_table, R,
+                                 q_per_req, max_pages_per_req, kv_bounds, gate, SV_LATENT_DIM, H,
+                                 softmax_scale, num_splits, workspace, workspace_bytes, out, lse,
+                                 status, stream);
 }
 
 extern "C" const char* sv_status_string(sv_status s) {

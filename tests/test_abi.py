@@ -149,3 +149,26 @@ def test_auto_split_choice(lib):
     assert num_splits_for(1, 8, 64, 24) >= 1       # one request: uniform splits
     assert num_splits_for(16, 8, 64, 512) == -1    # long contexts, one wave: balanced plan
     assert num_splits_for(32, 5, 64, 24) >= 1      # short contexts: uniform splits
+
+
+def test_gated_and_wuv_host_checks(lib):
+    args = dict(q=1 << 12, kv=1 << 12, num_pages=4, page_size=64, bt=1 << 12, R=2, qpr=4, maxp=2,
+                bounds=1 << 12, gate=1 << 12, H=8, scale=0.1, splits=1, ws=None, ws_bytes=0,
+                out=1 << 12, lse=1 << 12, status=None, stream=None)
+
+    def gated(gate_dim, **kw):
+        a = dict(args)
+        a.update(kw)
+        return lib.mla_verify_decode_gated(a["q"], a["kv"], a["num_pages"], a["page_size"], a["bt"], a["R"],
+                                           a["qpr"], a["maxp"], a["bounds"], a["gate"], gate_dim, a["H"],
+                                           ctypes.c_float(a["scale"]), a["splits"], a["ws"], a["ws_bytes"],
+                                           a["out"], a["lse"], a["status"], a["stream"])
+    assert gated(7) == 5          # gate_dim must be 512 or 1
+    assert gated(1, R=0) == 0
+    assert gated(1, q=None) == 1
+    f = lib.mla_wuv_project
+    assert f(4096, 4096, 4, 2, 100, 4096, None, None) == 5   # v_dim not a multiple of 32
+    assert f(4096, 4096, 4, 2, 512, 4096, None, None) == 5   # v_dim > 256
+    assert f(4096, 4096, 0, 2, 128, 4096, None, None) == 0
+    assert f(None, 4096, 4, 2, 128, 4096, None, None) == 1
+    assert f(4096 + 8, 4096, 4, 2, 128, 4096, None, None) == 3
