@@ -1,6 +1,7 @@
 """Float64 CPU oracle (test infrastructure only; never part of the product path)."""
 from .verify_ref import (  # noqa: F401
     bf16_bits_to_f64,
+    e4m3_bits_to_f64,
     gate_factor,
     gather_latent_rows,
     ref_attention_partials,

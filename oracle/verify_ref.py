@@ -34,6 +34,14 @@ What it computes, written as the plain definitions (no blocking, no fusion):
   v[t, h] = W_UV[h] @ out[t, h] ("LSE combine + W_UV" after the context-
   parallel merge, vLLM page "kimi_k3/nvidia/specialized_decode/drafter/
   model"; absorbed MLA keeps W_UV out of the attention).
+* fp8 latent KV (``e4m3_bits_to_f64``): a page pool of OCP FP8 E4M3 codes
+  (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; subnormals;
+  S.1111.111 is NaN, no infinities) with one scale for the whole pool; the
+  cached latent row is code value x kv_scale.  The attention over it is the
+  plain definition applied to those dequantised rows (the model card
+  "RedHatAI/Kimi-K3-speculator.dspark", section "Deployment", serves the
+  target with an fp8 KV cache; "TensorRT-LLM PR #18166" keeps fp8 KV out of
+  its verify kernel, so this is the "next" variant).
 * Split-KV partials and their merge (``ref_attention_partials``,
   ``ref_lse_combine``): each KV range gives (o_s, lse_s) by the same formula;
   lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s, and an all
@@ -64,6 +72,18 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns (uint16) to float64."""
     u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return u.view(np.float32).astype(np.float64)
+
+
+def e4m3_bits_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Exact value of FP8 E4M3 codes (uint8), from the format's definition."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = sign * (1.0 + m / 8.0) * np.power(2.0, e - 7)
+    sub = sign * (m / 8.0) * 2.0 ** -6
+    v = np.where(e == 0, sub, normal)
+    return np.where((c & 0x7F) == 0x7F, np.nan, v)
 
 
 def gather_latent_rows(kv_pages: np.ndarray, block_row: np.ndarray, n: int) -> np.ndarray:

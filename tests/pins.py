@@ -565,3 +565,48 @@ def pin_wuv_projection(orc):
 
 
 ALL_PINS += [pin_headwise_gate, pin_wuv_projection]
+
+
+# --------------------------------------------------------------------------
+# fp8 latent KV
+# --------------------------------------------------------------------------
+def pin_e4m3_decode(orc):
+    """The E4M3 decode against torch's float8_e4m3fn for all 256 codes, plus
+    hand values (largest normal 448, smallest subnormal 2^-9, NaN codes)."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).double().numpy()
+    got = orc.e4m3_bits_to_f64(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert orc.e4m3_bits_to_f64(np.array([0x7E]))[0] == 448.0
+    assert orc.e4m3_bits_to_f64(np.array([0x01]))[0] == 2.0 ** -9
+    assert orc.e4m3_bits_to_f64(np.array([0xB8]))[0] == -1.0
+    assert orc.e4m3_bits_to_f64(np.array([0x80]))[0] == 0.0
+
+
+def pin_fp8_attention_scale(orc):
+    """Attention over an fp8 pool is the attention over its dequantised rows;
+    the pool scale only rescales the scores and the output: with kv_scale s,
+    (softmax_scale, s) gives the same lse as (softmax_scale * s, 1) and s times
+    its output."""
+    inp = make_inputs("c0", seed=1)
+    from workloads import fp8_kv_pool
+    codes, s = fp8_kv_pool(inp)
+    k1 = inp["k"] + 1
+    deq = orc.e4m3_bits_to_f64(codes) * s
+    o1, l1 = orc.ref_verify_attention(inp["q_bits"], deq, inp["block_table"], inp["kv_bounds"],
+                                      inp["gate_bits"], k1, inp["softmax_scale"])
+    o2, l2 = orc.ref_verify_attention(inp["q_bits"], orc.e4m3_bits_to_f64(codes), inp["block_table"],
+                                      inp["kv_bounds"], inp["gate_bits"], k1, inp["softmax_scale"] * s)
+    fin = np.isfinite(l1)
+    assert np.array_equal(fin, np.isfinite(l2))
+    assert np.allclose(l1[fin], l2[fin], rtol=0, atol=1e-9)
+    assert np.allclose(o1, s * o2, rtol=1e-9, atol=1e-12)
+    # the quantised pool stays close to the bf16 one (|error| <= 2^-4 relative + subnormal step)
+    bf = orc.bf16_bits_to_f64(inp["kv_bits"])
+    assert np.all(np.abs(deq - bf) <= np.abs(bf) / 16 + s * 2.0 ** -10)
+
+
+ALL_PINS += [pin_e4m3_decode, pin_fp8_attention_scale]

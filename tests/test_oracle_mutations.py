@@ -153,7 +153,13 @@ def _mut_wuv_transposed_input(m):
     m.ref_wuv_project = f
 
 
+def _mut_e4m3_bias(m):
+    orig = m.e4m3_bits_to_f64
+    m.e4m3_bits_to_f64 = lambda c: orig(c) * 0.5  # exponent bias 8 instead of 7
+
+
 MUTATIONS = [
+    _mut_e4m3_bias,
     _mut_wuv_wrong_head, _mut_headwise_gate_ignored, _mut_wuv_transposed_input,
     _mut_bound_off_by_one, _mut_no_scale, _mut_gate_sign, _mut_token_mapping, _mut_lse_log2,
     _mut_argmax_last, _mut_draft_position, _mut_trim, _mut_unnormalised_merge, _mut_nan_identity,

@@ -252,6 +252,19 @@ def make_sampled_inputs(cfg: VerifyConfig | str, seed: int = 0, temperature: flo
                 draft_probs=draft_probs, draft_tokens=drafts, uniforms=uniforms)
 
 
+def fp8_kv_pool(inp: dict, amax_target: float = 448.0) -> tuple[np.ndarray, float]:
+    """An FP8 E4M3 page pool for the batch of ``make_inputs``: the bf16 latent
+    rows scaled by 1 / kv_scale (kv_scale = max |row value| / 448, so the pool
+    spans the format's range) and rounded to the nearest E4M3 code (torch's
+    float8_e4m3fn conversion).  Returns (codes uint8 [P][64][512], kv_scale)."""
+    import torch
+    kv = torch.from_numpy(np.ascontiguousarray(inp["kv_bits"]).view(np.int16)).view(torch.bfloat16).float()
+    amax = float(kv.abs().max())
+    kv_scale = amax / amax_target if amax > 0 else 1.0
+    codes = (kv / kv_scale).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return codes, float(kv_scale)
+
+
 def small_config(base: str | VerifyConfig = "c0", **overrides) -> VerifyConfig:
     """A variant of a named configuration (edge cases, test sweeps)."""
     if isinstance(base, str):
