@@ -334,6 +334,17 @@ def main():
                                                       temperature=sinp["temperature"], workspace=s_ws,
                                                       accepted=s_out[0], next_tokens=s_out[1],
                                                       kv_lens_out=s_out[2]), args.steps)
+    # the same attention over an fp8 (E4M3 + scale) copy of the KV pool
+    from workloads import fp8_kv_pool
+    codes, kv_scale = fp8_kv_pool(inp)
+    kv8 = torch.from_numpy(codes).to(device)
+    out8 = torch.empty_like(step.out)
+    lse8 = torch.empty_like(step.lse)
+    kv8_ms = timed(lambda: sv.mla_verify_decode(q, kv8, bt, bounds, gate, k + 1, inp["softmax_scale"],
+                                                num_splits=step.num_splits, workspace=step.attn_ws,
+                                                out=out8, lse=lse8, status=step.status, kv_scale=kv_scale),
+                   args.steps)
+    del kv8
     # per-head W_UV value up-projection of the attention output (v_dim 128,
     # seeded bf16 weights), the step after the merge
     from workloads import f32_to_bf16_bits
@@ -378,6 +389,7 @@ def main():
     append_mean = agg(append_ms)
     sampled_mean = agg(sampled_ms)
     wuv_mean = agg(wuv_ms)
+    kv8_mean = agg(kv8_ms)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -431,6 +443,8 @@ def main():
         "kv_append_gbps": T * 2 * 1024 / (append_mean * 1e-3) / 1e9,
         "sampled_verify_us": sampled_mean * 1000.0,
         "sampled_verify_gbps": (T + 2 * R) * V * 4 / (sampled_mean * 1e-3) / 1e9,
+        "attention_kv8_us": kv8_mean * 1000.0,
+        "attention_kv8_tflops": attn_flops / (kv8_mean * 1e-3) / 1e12,
         "wuv_project_us": wuv_mean * 1000.0,
         "wuv_project_tflops": 2.0 * T * H * 128 * 512 / (wuv_mean * 1e-3) / 1e12,
         "steps_per_s_all_gpus": replica_throughput(step_mean, world),
@@ -440,7 +454,7 @@ def main():
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * step.launches_per_step,
         "gpu_launches_all_timed_loops": args.steps * (2 * step.launches_per_step + step.attention_launches
-                                                       + 1 + 1 + 2 + 1),
+                                                       + 1 + 1 + 2 + 1 + step.attention_launches),
         "clocks": clocks,
         "status_word": int(step.status.item()),
     }

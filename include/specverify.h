@@ -12,6 +12,7 @@
  *                       the LSE merge and the sigmoid gate fused in.
  *   mla_lse_combine     the LSE merge + gate of split partials on its own.
  *   mla_verify_decode_gated  the same with a head-wise ([T][H]) gate.
+ *   mla_verify_decode_kv8    the same over an fp8 (E4M3 + scale) page pool.
  *   mla_wuv_project     the per-head W_UV value up-projection after the merge.
  *   mla_kv_append       the verify tokens' latent rows into the paged cache.
  *   spec_verify_sampled rejection-sampling verification (probabilistic drafts).
@@ -169,6 +170,26 @@ sv_status mla_verify_decode_gated(const void* q_latent, const void* kv_pages, in
                                   const void* gate, int gate_dim, int H, float softmax_scale,
                                   int num_splits, void* workspace, size_t workspace_bytes,
                                   void* out, float* lse, int32_t* status, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * mla_verify_decode_kv8
+ *
+ * mla_verify_decode_gated over an fp8 latent KV cache (the fp8 KV deployment
+ * on the model card "RedHatAI/Kimi-K3-speculator.dspark", section
+ * "Deployment"; the verify kernel of "TensorRT-LLM PR #18166" rejects fp8 KV,
+ * so this is the "next" variant): kv_pages_e4m3 holds OCP FP8 E4M3 codes
+ * [num_pages][64][512] (1 byte each, 16-byte aligned) and the cached latent
+ * row is code value * kv_scale (one scale for the pool, finite and > 0).
+ * The kernel converts each tile to bf16 in shared memory (exact) and folds
+ * kv_scale into the score scale and the output.  Everything else as
+ * mla_verify_decode_gated; the workspace query is the same.
+ * ---------------------------------------------------------------------- */
+sv_status mla_verify_decode_kv8(const void* q_latent, const void* kv_pages_e4m3, float kv_scale,
+                                int num_pages, int page_size, const int32_t* block_table, int R,
+                                int q_per_req, int max_pages_per_req, const int32_t* kv_bounds,
+                                const void* gate, int gate_dim, int H, float softmax_scale,
+                                int num_splits, void* workspace, size_t workspace_bytes,
+                                void* out, float* lse, int32_t* status, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * mla_wuv_project

@@ -42,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "spec_verify_sampled",
     "mla_verify_decode_gated",
     "mla_wuv_project",
+    "mla_verify_decode_kv8",
 )
 
 _lib = None
@@ -103,6 +104,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.mla_wuv_project.argtypes = [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_void_p,
                                         _c_void_p, _c_void_p]
         lib.mla_wuv_project.restype = _c_int
+        lib.mla_verify_decode_kv8.argtypes = [
+            _c_void_p, _c_void_p, _c_float, _c_int, _c_int, _c_void_p, _c_int, _c_int, _c_int,
+            _c_void_p, _c_void_p, _c_int, _c_int, _c_float, _c_int, _c_void_p, _c_size,
+            _c_void_p, _c_void_p, _c_void_p, _c_void_p]
+        lib.mla_verify_decode_kv8.restype = _c_int
         _lib = lib
         return lib
 
@@ -145,16 +151,20 @@ def mla_verify_decode(q_latent: torch.Tensor, kv_pages: torch.Tensor, block_tabl
                       kv_bounds: torch.Tensor, gate: torch.Tensor, q_per_req: int,
                       softmax_scale: float, num_splits: int = 0,
                       workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
-                      lse: torch.Tensor | None = None, status: torch.Tensor | None = None):
-    """Gated NoPE MLA verify attention.  Shapes: q_latent/gate [T, H, 512] bf16,
-    kv_pages [P, 64, 512] bf16, block_table [R, max_pages] int32, kv_bounds [T]
+                      lse: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                      kv_scale: float | None = None):
+    """Gated NoPE MLA verify attention.  Shapes: q_latent [T, H, 512] bf16,
+    gate [T, H, 512] or [T, H] bf16, kv_pages [P, 64, 512] bf16 (or uint8 E4M3
+    codes with kv_scale given), block_table [R, max_pages] int32, kv_bounds [T]
     int32.  Returns (out [T, H, 512] bf16, lse [T, H] fp32)."""
     lib = load_library()
     _check(q_latent.dim() == 3 and q_latent.shape[2] == SV_LATENT_DIM, "q_latent must be [T, H, 512]")
     T, H, _ = q_latent.shape
     dev = q_latent.device
     _check(dev.type == "cuda", "tensors must live on a CUDA device")
-    for name, t, dt in (("q_latent", q_latent, torch.bfloat16), ("kv_pages", kv_pages, torch.bfloat16),
+    kv8 = kv_scale is not None
+    for name, t, dt in (("q_latent", q_latent, torch.bfloat16),
+                        ("kv_pages", kv_pages, torch.uint8 if kv8 else torch.bfloat16),
                         ("gate", gate, torch.bfloat16), ("block_table", block_table, torch.int32),
                         ("kv_bounds", kv_bounds, torch.int32)):
         _check(t.dtype == dt, f"{name} must be {dt}")
@@ -178,11 +188,18 @@ def mla_verify_decode(q_latent: torch.Tensor, kv_pages: torch.Tensor, block_tabl
     if ws_bytes > 0 and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     ws_size = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    code = lib.mla_verify_decode_gated(
-        _ptr(q_latent), _ptr(kv_pages), int(kv_pages.shape[0]), int(kv_pages.shape[1]),
-        _ptr(block_table), R, q_per_req, max_pages, _ptr(kv_bounds), _ptr(gate), gate_dim, H,
-        float(softmax_scale), int(num_splits), _ptr(workspace), ws_size, _ptr(out), _ptr(lse),
-        _ptr(status), _stream(dev))
+    if kv8:
+        code = lib.mla_verify_decode_kv8(
+            _ptr(q_latent), _ptr(kv_pages), float(kv_scale), int(kv_pages.shape[0]),
+            int(kv_pages.shape[1]), _ptr(block_table), R, q_per_req, max_pages, _ptr(kv_bounds),
+            _ptr(gate), gate_dim, H, float(softmax_scale), int(num_splits), _ptr(workspace), ws_size,
+            _ptr(out), _ptr(lse), _ptr(status), _stream(dev))
+    else:
+        code = lib.mla_verify_decode_gated(
+            _ptr(q_latent), _ptr(kv_pages), int(kv_pages.shape[0]), int(kv_pages.shape[1]),
+            _ptr(block_table), R, q_per_req, max_pages, _ptr(kv_bounds), _ptr(gate), gate_dim, H,
+            float(softmax_scale), int(num_splits), _ptr(workspace), ws_size, _ptr(out), _ptr(lse),
+            _ptr(status), _stream(dev))
     _check_status("mla_verify_decode", code)
     return out, lse
 

@@ -63,30 +63,44 @@ constexpr int kD = SV_LATENT_DIM;
 constexpr int kDHalf = kD / 2;
 constexpr int kTileN = SV_PAGE_SIZE;  // KV rows per tile = one page
 constexpr int kMTile = 128;           // folded query rows per unit
-constexpr int kOwnStages = 3;
-constexpr int kOthStages = 2;
 constexpr int kBoxBytes = 64 * 128;            // one KV TMA box: 64 rows x 64 bf16
 constexpr int kHalfTileBytes = 4 * kBoxBytes;  // 64 rows x 256 bf16
 constexpr int kQBoxBytes = 128 * 128;          // one Q TMA box: 128 rows x 64 bf16
 constexpr int kQHalfBytes = 4 * kQBoxBytes;    // 128 rows x 256 bf16
-constexpr int kThreads = 192;
-constexpr int kNumBars = 19;
 constexpr uint32_t kEpilogueBarId = 1;  // named barrier of the softmax warps
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS = 384, kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // in log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
-// shared memory map (offsets from the 1024-aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffOwn = kOffQ + kQHalfBytes;
-constexpr int kOffOth = kOffOwn + kOwnStages * kHalfTileBytes;
-constexpr int kOffBar = kOffOth + kOthStages * kHalfTileBytes;
-constexpr int kSmemUsed = kOffBar + kNumBars * 8 + 16;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffOth == kOffOwn + kOwnStages * kHalfTileBytes &&
-                  kOwnStages * kHalfTileBytes + kOthStages * kHalfTileBytes >= 8 * kQBoxBytes,
-              "the epilogue stages a 128 x 256 fp32 tile over the two KV rings");
+constexpr int kF8TileBytes = 64 * kD;  // one fp8 KV tile: 64 rows x 512 e4m3 codes
+
+// Two variants of the kernel.  bf16 KV: the TMA producer fills the bf16 KV
+// rings.  fp8 KV: four converter warps (warps 6..9) read each e4m3 tile from
+// global memory one tile ahead into registers (coalesced 16-byte loads) and
+// write it as bf16 into the same swizzled ring slots the MMAs read (e4m3 ->
+// bf16 is exact); the producer then only loads the query half.
+template <bool kF8>
+struct KernelShape {
+  static constexpr int kOwnStages = 3;
+  static constexpr int kOthStages = 2;
+  static constexpr int kF8Stages = 0;
+  static constexpr int kThreads = kF8 ? 320 : 192;
+  static constexpr int kNumBars = 19;
+  static constexpr int kFullCount = kF8 ? 128 : 1;  // arrivals completing a KV ring slot
+  // shared memory map (offsets from the 1024-aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffOwn = kOffQ + kQHalfBytes;
+  static constexpr int kOffOth = kOffOwn + kOwnStages * kHalfTileBytes;
+  static constexpr int kOffF8 = kOffOth + kOthStages * kHalfTileBytes;
+  static constexpr int kOffBar = kOffF8 + kF8Stages * kF8TileBytes;
+  static constexpr int kSmemUsed = kOffBar + kNumBars * 8 + 16;
+  static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+};
+static_assert(KernelShape<false>::kSmemBytes <= 232448 && KernelShape<true>::kSmemBytes <= 232448,
+              "shared memory budget");
+static_assert(KernelShape<false>::kOffBar - KernelShape<false>::kOffOwn >= 8 * kQBoxBytes &&
+                  KernelShape<true>::kOffBar - KernelShape<true>::kOffOwn >= 8 * kQBoxBytes,
+              "the epilogue stages a 128 x 256 fp32 tile over the idle KV buffers");
 
 struct VerifyParams {
   const __nv_bfloat16* q;
@@ -107,7 +121,20 @@ struct VerifyParams {
   const int* plan_header;
   long long part_w_stride;  // part_lse elements between consecutive slots
   int gate_dim;             // 512: elementwise gate [T][H][512]; 1: head-wise gate [T][H]
+  float kv_scale;           // fp8 KV: the pool's scale (1 for bf16 KV)
+  const uint8_t* kv8;       // fp8 KV: the e4m3 page pool [pages][64][512]
 };
+
+// Two e4m3 codes (low byte first) -> two bf16 (low half first); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
+  float lo, hi;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+  return pack_bf16x2(lo, hi);
+}
 
 __device__ __forceinline__ int load_bound(const VerifyParams& p, int tok) {
   int b = __ldg(p.kv_bounds + tok);
@@ -137,12 +164,16 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // Tensor maps: tmap_kv 2-D over the page pool [pages*64][512] bf16; tmap_q,
 // tmap_gate, tmap_out 3-D [R][M][512] bf16 (rows past a request's M fall out
 // of bounds: zero on load, dropped on store); tmap_part 4-D [S][R][M][512] fp32.
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kF8>
+__global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
     mla_verify_kernel(const __grid_constant__ CUtensorMap tmap_kv,
                       const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_gate,
                       const __grid_constant__ CUtensorMap tmap_out,
                       const __grid_constant__ CUtensorMap tmap_part, const VerifyParams p) {
+  using K = KernelShape<kF8>;
+  constexpr int kOwnStages = K::kOwnStages, kOthStages = K::kOthStages, kNumBars = K::kNumBars;
+  constexpr int kOffQ = K::kOffQ, kOffOwn = K::kOffOwn, kOffOth = K::kOffOth, kOffBar = K::kOffBar;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -214,13 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kOwnStages; ++s) {
-      mbar_init(own_full(s), 1);
+      mbar_init(own_full(s), K::kFullCount);
       mbar_init(own_empty(s), 1);
     }
     for (int s = 0; s < kOthStages; ++s) {
-      mbar_init(oth_full(s), 1);
+      mbar_init(oth_full(s), K::kFullCount);
       mbar_init(oth_empty(s), 1);
     }
+
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
       mbar_init(p_full(b), 128);
@@ -270,8 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int b = 0; b < 4; ++b)
         tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_ready, (1 - half) * kDHalf + b * 64,
                     m_tile * kMTile, r);
-      int last_own[kOwnStages] = {-1, -1, -1};
-      int last_oth[kOthStages] = {-1, -1};
+      if constexpr (!kF8) {
+      int last_own[kOwnStages];
+      int last_oth[kOthStages];
+      for (int s = 0; s < kOwnStages; ++s) last_own[s] = -1;
+      for (int s = 0; s < kOthStages; ++s) last_oth[s] = -1;
       for (int it = 0; it < ntiles; ++it) {
         const int j = lo + it;
         int page = __ldg(p.block_table + (long long)r * p.max_pages + j);
@@ -306,6 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last_own[s] >= 0) drain_wait(own_full(s), last_own[s] & 1);
       for (int s = 0; s < kOthStages; ++s)
         if (last_oth[s] >= 0) drain_wait(oth_full(s), last_oth[s] & 1);
+      } else {
+        // fp8 KV: the converter warps fill the KV rings; only the query copy
+        // has to land before teardown
+        drain_wait(q_ready, 0);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -397,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(drain_bar, 0);
     }
     __syncwarp();
-  } else {
+  } else if (!kF8 || warp < 6) {
     // ------------------------------------------------------------ softmax + epilogue
     const int wq = warp & 3;  // TMEM lane quadrant of this warp
     const int i = wq * 32 + lane;
@@ -518,7 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(pv_done((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
     tc_fence_after();
     const bool have_o = ok && ntiles > 0;
-    const float inv_l = (l_sum > 0.f) ? 1.0f / l_sum : 0.f;
+    float inv_l = (l_sum > 0.f) ? 1.0f / l_sum : 0.f;
+    if constexpr (kF8) inv_l *= p.kv_scale;  // o of the codes -> o of the rows
     const float lse_v = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
     // staging: the KV rings are idle once the last P V has completed
     uint8_t* const stage = sptr + kOffOwn;
@@ -605,6 +646,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_store_wait_read();  // SMEM stays valid until the stores have read it
     }
     __syncwarp();
+  }
+
+  if constexpr (kF8) {
+    if (warp >= 6) {
+      // ---------------------------------------------------------- fp8 converters
+      // 128 threads: tile it's 64 x 512 codes are loaded into registers while
+      // tile it-1 is converted (thread ct holds 16 chunks of 16 codes: row
+      // 4k + ct/32, columns 16 (ct%32) .. +15), then written as bf16 into the
+      // own / other ring slots of tile it, swizzled like a TMA box.
+      const int ct = threadIdx.x - 192;
+      const int32_t* bt_row = p.block_table + (long long)r * p.max_pages + lo;
+      uint4 buf[16];
+      auto load_tile = [&](int it) {
+        int page = __ldg(bt_row + it);
+        if (page < 0 || page >= p.num_pages) {
+          if (ct == 0 && p.status) atomicOr(p.status, SV_DEV_BAD_PAGE);
+          page = 0;
+        }
+        const uint4* base = reinterpret_cast<const uint4*>(p.kv8 + (long long)page * kTileN * kD);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) buf[k] = __ldcs(base + (k * 128 + ct));
+      };
+      if (ntiles > 0) load_tile(0);
+      bool ok = true;
+      for (int it = 0; ok && it < ntiles; ++it) {
+        const int so = it % kOwnStages, ro = it / kOwnStages;
+        const int sx = it % kOthStages, rx = it / kOthStages;
+        if (ro > 0) ok = mbar_wait<false>(own_empty(so), (ro - 1) & 1, abort_flag, p.status);
+        if (ok && rx > 0) ok = mbar_wait<false>(oth_empty(sx), (rx - 1) & 1, abort_flag, p.status);
+        if (!ok) break;
+        uint8_t* const own_t = sptr + kOffOwn + so * kHalfTileBytes;
+        uint8_t* const oth_t = sptr + kOffOth + sx * kHalfTileBytes;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int c = k * 128 + ct;
+          const int row = c >> 5, g = c & 31;  // 16-column group g of row `row`
+          const uint4 v = buf[k];
+          const int col = g * 16;
+          uint8_t* const ring = ((col >> 8) == half) ? own_t : oth_t;
+          const int b = (col & 255) >> 6;
+          const int j0 = (col & 63) >> 3;  // 16-byte chunks j0, j0+1 of the 128-byte row
+          uint4 w0, w1;
+          w0.x = e4m3x2_to_bf16x2(v.x);
+          w0.y = e4m3x2_to_bf16x2(v.x >> 16);
+          w0.z = e4m3x2_to_bf16x2(v.y);
+          w0.w = e4m3x2_to_bf16x2(v.y >> 16);
+          w1.x = e4m3x2_to_bf16x2(v.z);
+          w1.y = e4m3x2_to_bf16x2(v.z >> 16);
+          w1.z = e4m3x2_to_bf16x2(v.w);
+          w1.w = e4m3x2_to_bf16x2(v.w >> 16);
+          uint8_t* const rb = ring + b * kBoxBytes + row * 128;
+          *reinterpret_cast<uint4*>(rb + (((uint32_t)j0 ^ (uint32_t)(row & 7)) << 4)) = w0;
+          *reinterpret_cast<uint4*>(rb + (((uint32_t)(j0 + 1) ^ (uint32_t)(row & 7)) << 4)) = w1;
+        }
+        fence_proxy_async_smem();  // the tensor cores read what the threads wrote
+        mbar_arrive(own_full(so));
+        mbar_arrive(oth_full(sx));
+        if (it + 1 < ntiles) load_tile(it + 1);
+      }
+    }
   }
 
   // ---- teardown (every warp is converged here)
@@ -794,8 +895,10 @@ bool device_setup(int* sm_count) {
   if (!g_attr_set[dev]) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-    if (cudaFuncSetAttribute(mla_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(mla_verify_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KernelShape<false>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_verify_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KernelShape<true>::kSmemBytes) != cudaSuccess)
       return false;
     g_sm_count[dev] = sms;
     g_attr_set[dev] = true;
@@ -887,15 +990,16 @@ extern "C" size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits) {
   return o_bytes + (size_t)num_splits * rows * sizeof(float);
 }
 
-extern "C" sv_status mla_verify_decode_gated(const void* q_latent, const void* kv_pages,
-                                             int num_pages, int page_size,
-                                             const int32_t* block_table, int R, int q_per_req,
-                                             int max_pages_per_req, const int32_t* kv_bounds,
-                                             const void* gate, int gate_dim, int H,
-                                             float softmax_scale, int num_splits, void* workspace,
-                                             size_t workspace_bytes, void* out, float* lse,
-                                             int32_t* status, sv_stream_t stream) {
-  using namespace sv;
+namespace sv {
+namespace {
+// The attention call for both KV formats: kv_fp8 selects an e4m3 page pool
+// with scale kv_scale (the fp8 kernel variant), else a bf16 pool.
+sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, float kv_scale,
+                      int num_pages, int page_size, const int32_t* block_table, int R,
+                      int q_per_req, int max_pages_per_req, const int32_t* kv_bounds,
+                      const void* gate, int gate_dim, int H, float softmax_scale, int num_splits,
+                      void* workspace, size_t workspace_bytes, void* out, float* lse,
+                      int32_t* status, sv_stream_t stream) {
   if (R < 0 || q_per_req < 1 || H < 1 || max_pages_per_req < 0 || num_pages < 0)
     return SV_ERR_SHAPE;
   if (gate_dim != kD && gate_dim != 1) return SV_ERR_UNSUPPORTED;
@@ -907,6 +1011,7 @@ extern "C" sv_status mla_verify_decode_gated(const void* q_latent, const void* k
   if (T == 0) return SV_OK;
   if (T * H > 0x7FFFFFFFll || (long long)num_pages * kTileN > 0x7FFFFFFFll) return SV_ERR_SHAPE;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return SV_ERR_SHAPE;
+  if (kv_fp8 && (!(kv_scale > 0.f) || !std::isfinite(kv_scale))) return SV_ERR_SHAPE;
   if (num_pages < 1 || max_pages_per_req < 1) return SV_ERR_SHAPE;
   if (!q_latent || !kv_pages || !block_table || !kv_bounds || !gate || !out || !lse)
     return SV_ERR_NULL;
@@ -952,7 +1057,9 @@ extern "C" sv_status mla_verify_decode_gated(const void* q_latent, const void* k
     const cuuint64_t row_dims[3] = {(cuuint64_t)kD, (cuuint64_t)Mq, (cuuint64_t)R};
     const cuuint32_t row_box[3] = {64, (cuuint32_t)kMTile, 1};
     const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!encode_map(&tmap_kv, bf16, 2, kv_pages, 2, kv_dims, kv_box) ||
+    // fp8 KV is read by the converter warps, not through a tensor map
+    if ((kv_fp8 ? !encode_map(&tmap_kv, bf16, 2, q_latent, 3, row_dims, row_box)
+                : !encode_map(&tmap_kv, bf16, 2, kv_pages, 2, kv_dims, kv_box)) ||
         !encode_map(&tmap_q, bf16, 2, q_latent, 3, row_dims, row_box) ||
         (gate_dim == kD ? !encode_map(&tmap_gate, bf16, 2, gate, 3, row_dims, row_box)
                         : !encode_map(&tmap_gate, bf16, 2, q_latent, 3, row_dims, row_box)) ||
@@ -996,13 +1103,21 @@ extern "C" sv_status mla_verify_decode_gated(const void* q_latent, const void* k
   prm.plan_header = nullptr;
   prm.part_w_stride = T * H;
   prm.gate_dim = gate_dim;
+  prm.kv_scale = kv_fp8 ? kv_scale : 1.0f;
+  prm.kv8 = kv_fp8 ? static_cast<const uint8_t*>(kv_pages) : nullptr;
+  // fp8: the pool scale multiplies every score (folded into the scale here)
+  // and the output (applied in the epilogue)
+  if (kv_fp8) prm.scale_log2 *= kv_scale;
+  auto kernel = kv_fp8 ? mla_verify_kernel<true> : mla_verify_kernel<false>;
+  const int threads = kv_fp8 ? KernelShape<true>::kThreads : KernelShape<false>::kThreads;
+  const int smem = kv_fp8 ? KernelShape<true>::kSmemBytes : KernelShape<false>::kSmemBytes;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   if (!balanced) {
     const long long ctas = 2ll * R * prm.n_mtiles * S;
     if (ctas > 0x7FFFFFFFll) return SV_ERR_SHAPE;
-    mla_verify_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, st>>>(tmap_kv, tmap_q, tmap_gate,
-                                                                   tmap_out, tmap_part, prm);
+    kernel<<<(unsigned)ctas, threads, smem, st>>>(tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part,
+                                                  prm);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_LAUNCH;
     if (S > 1 && launch_lse_combine(part_o, part_lse, S, T * H, gate, out, lse, st, nullptr,
                                     nullptr, 1, gate_dim) != cudaSuccess)
@@ -1025,15 +1140,15 @@ extern "C" sv_status mla_verify_decode_gated(const void* q_latent, const void* k
   prm.part_w_stride = Mq_ll;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)PL.units_max, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, mla_verify_kernel, tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part,
+  if (cudaLaunchKernelEx(&cfg, kernel, tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part,
                          prm) != cudaSuccess) {
     cudaGetLastError();
     return SV_ERR_LAUNCH;
@@ -1042,6 +1157,36 @@ extern "C" sv_status mla_verify_decode_gated(const void* q_latent, const void* k
                          (int)Mq_ll, gate_dim) != cudaSuccess)
     return SV_ERR_LAUNCH;
   return SV_OK;
+}
+}  // namespace
+}  // namespace sv
+
+extern "C" sv_status mla_verify_decode_gated(const void* q_latent, const void* kv_pages,
+                                             int num_pages, int page_size,
+                                             const int32_t* block_table, int R, int q_per_req,
+                                             int max_pages_per_req, const int32_t* kv_bounds,
+                                             const void* gate, int gate_dim, int H,
+                                             float softmax_scale, int num_splits, void* workspace,
+                                             size_t workspace_bytes, void* out, float* lse,
+                                             int32_t* status, sv_stream_t stream) {
+  return sv::verify_impl(q_latent, kv_pages, false, 1.0f, num_pages, page_size, block_table, R,
+                         q_per_req, max_pages_per_req, kv_bounds, gate, gate_dim, H,
+                         softmax_scale, num_splits, workspace, workspace_bytes, out, lse, status,
+                         stream);
+}
+
+extern "C" sv_status mla_verify_decode_kv8(const void* q_latent, const void* kv_pages_e4m3,
+                                           float kv_scale, int num_pages, int page_size,
+                                           const int32_t* block_table, int R, int q_per_req,
+                                           int max_pages_per_req, const int32_t* kv_bounds,
+                                           const void* gate, int gate_dim, int H,
+                                           float softmax_scale, int num_splits, void* workspace,
+                                           size_t workspace_bytes, void* out, float* lse,
+                                           int32_t* status, sv_stream_t stream) {
+  return sv::verify_impl(q_latent, kv_pages_e4m3, true, kv_scale, num_pages, page_size,
+                         block_table, R, q_per_req, max_pages_per_req, kv_bounds, gate, gate_dim,
+                         H, softmax_scale, num_splits, workspace, workspace_bytes, out, lse,
+                         status, stream);
 }
 
 extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_pages, int num_pages,

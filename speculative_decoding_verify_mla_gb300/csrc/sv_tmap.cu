@@ -24,7 +24,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }
 
 bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base,
-                int rank, const cuuint64_t* dims, const cuuint32_t* box) {
+                int rank, const cuuint64_t* dims, const cuuint32_t* box,
+                CUtensorMapSwizzle swizzle) {
   auto encode = get_encode_fn();
   if (!encode || rank < 1 || rank > 5) return false;
   cuuint64_t strides[4];
@@ -35,7 +36,7 @@ bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, con
   }
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return encode(map, dtype, rank, const_cast<void*>(base), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -172,3 +172,20 @@ def test_gated_and_wuv_host_checks(lib):
     assert f(4096, 4096, 0, 2, 128, 4096, None, None) == 0
     assert f(None, 4096, 4, 2, 128, 4096, None, None) == 1
     assert f(4096 + 8, 4096, 4, 2, 128, 4096, None, None) == 3
+
+
+def test_kv8_host_checks(lib):
+    f = lib.mla_verify_decode_kv8
+    fl = ctypes.c_float
+    base = [1 << 12, 1 << 12, fl(0.5), 4, 64, 1 << 12, 2, 4, 2, 1 << 12, 1 << 12, 512, 8, fl(0.1), 1,
+            None, 0, 1 << 12, 1 << 12, None, None]
+    a = list(base); a[2] = fl(0.0)
+    assert f(*a) == 2            # kv_scale must be > 0
+    a = list(base); a[2] = fl(float("nan"))
+    assert f(*a) == 2
+    a = list(base); a[4] = 32
+    assert f(*a) == 5            # page size
+    a = list(base); a[1] = None
+    assert f(*a) == 1
+    a = list(base); a[6] = 0
+    assert f(*a) == 0            # no requests
