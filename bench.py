@@ -311,6 +311,23 @@ def main():
                                                     argmax_ids=step.argmax, accepted=step.accepted,
                                                     next_tokens=step.next_tokens,
                                                     kv_lens_out=step.kv_lens_out), args.steps)
+    # the same step replayed from a CUDA graph (launch overheads removed)
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=device)
+        cap.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                run_step()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        graph_ms = timed(g.replay, args.steps)
+    except RuntimeError as e:  # capture unsupported by this torch/driver: reported, not hidden
+        graph_error = str(e).splitlines()[0][:120]
+    barrier()
     # paged latent KV append of the k+1 verify rows (the step just before the
     # attention); it rewrites the rows the pool already holds at those
     # positions, so the attention inputs stay the same
@@ -390,6 +407,7 @@ def main():
     sampled_mean = agg(sampled_ms)
     wuv_mean = agg(wuv_ms)
     kv8_mean = agg(kv8_ms)
+    graph_mean = agg(graph_ms) if graph_ms else None
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -443,6 +461,7 @@ def main():
         "kv_append_gbps": T * 2 * 1024 / (append_mean * 1e-3) / 1e9,
         "sampled_verify_us": sampled_mean * 1000.0,
         "sampled_verify_gbps": (T + 2 * R) * V * 4 / (sampled_mean * 1e-3) / 1e9,
+        "step_graph_replay_us": graph_mean * 1000.0 if graph_mean else None,
         "attention_kv8_us": kv8_mean * 1000.0,
         "attention_kv8_tflops": attn_flops / (kv8_mean * 1e-3) / 1e12,
         "wuv_project_us": wuv_mean * 1000.0,
@@ -453,7 +472,7 @@ def main():
         "e2e": {"value": e2e_mean * 1000.0, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * step.launches_per_step,
-        "gpu_launches_all_timed_loops": args.steps * (2 * step.launches_per_step + step.attention_launches
+        "gpu_launches_all_timed_loops": args.steps * (3 * step.launches_per_step + step.attention_launches
                                                        + 1 + 1 + 2 + 1 + step.attention_launches),
         "clocks": clocks,
         "status_word": int(step.status.item()),
