@@ -66,10 +66,23 @@ __global__ void __launch_bounds__(kCombineThreads)
     rin = row - rq * Mq;
   }
 
-  // split weights: lane s holds lse_s for s = lane and lane + 32
+  // split weights: lane s holds lse_s for s = lane and lane + 32.  The
+  // partials of the first kFirst splits are loaded in the same round trip
+  // (every split's partial is written, as zeros when its range is empty, so
+  // they can be read before the weights are known).
+  constexpr int kFirst = 12;
   float l0 = -INFINITY, l1 = -INFINITY;
   if (lane < S) l0 = ld_dep_f32(part_lse + (slot0 + lane) * slot_rows + rin);
   if (lane + 32 < S) l1 = ld_dep_f32(part_lse + (slot0 + lane + 32) * slot_rows + rin);
+  float4 v0[kFirst][2];
+#pragma unroll
+  for (int u = 0; u < kFirst; ++u) {
+    const float* src = part_o + ((slot0 + min(u, S - 1)) * slot_rows + rin) * 512 + col0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      v0[u][j] = (u < S) ? ld_dep_f4_stream(reinterpret_cast<const float4*>(src + 128 * j))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float m = fmaxf(l0, l1);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -84,8 +97,20 @@ __global__ void __launch_bounds__(kCombineThreads)
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
     const float inv_z = 1.0f / z;
     lse_row = m + __logf(z);
-    // eight splits per round: all their loads are in flight before any FMA
-    for (int s0 = 0; s0 < S; s0 += 8) {
+#pragma unroll
+    for (int u = 0; u < kFirst; ++u) {
+      const float ws = (u < S) ? __shfl_sync(0xFFFFFFFFu, w0, u) * inv_z : 0.f;
+      if (ws == 0.f) continue;  // an empty split's values are never used (0 * NaN stays out)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        acc[j].x = fmaf(ws, v0[u][j].x, acc[j].x);
+        acc[j].y = fmaf(ws, v0[u][j].y, acc[j].y);
+        acc[j].z = fmaf(ws, v0[u][j].z, acc[j].z);
+        acc[j].w = fmaf(ws, v0[u][j].w, acc[j].w);
+      }
+    }
+    // further splits, eight per round: all their loads in flight before any FMA
+    for (int s0 = kFirst; s0 < S; s0 += 8) {
       float4 v[8][2];
       float ws[8];
 #pragma unroll

@@ -414,3 +414,20 @@ def test_balanced_plan_head_shapes(sv, H, k, lens):
     ref_o, ref_l = oracle_attention(inp)
     out, lse = run_attention(sv, inp, num_splits=sv.SV_SPLITS_BALANCED)
     check_attention(out, lse, ref_o, ref_l, label=f"balanced H={H} k={k}")
+
+
+def test_combine_ignores_values_of_empty_splits(sv):
+    """A split with lse = -inf has weight 0; whatever its o holds (NaN here)
+    must not reach the output (0 * NaN would poison the row)."""
+    cfg = small_config("c0", R=2, k=3, H=16, kv_lens=(150, 260))
+    inp = make_inputs(cfg, seed=9)
+    edges = [[0, 150, 150, 150], [0, 0, 200, 260]]
+    po, pl = oracle.ref_attention_partials(inp["q_bits"], inp["kv_bits"], inp["block_table"], inp["kv_bounds"], 4,
+                                           inp["softmax_scale"], edges)
+    ref_o, ref_l = oracle.ref_lse_combine(po, pl, inp["gate_bits"])
+    po_nan = po.copy()
+    po_nan[~np.isfinite(pl)] = np.nan
+    out, lse = sv.mla_lse_combine(torch.from_numpy(po_nan.astype(np.float32)).to(DEV),
+                                  torch.from_numpy(pl.astype(np.float32)).to(DEV), bf16_tensor(inp["gate_bits"], DEV))
+    torch.cuda.synchronize()
+    check_attention(out, lse, ref_o, ref_l, label="combine with NaN in empty splits")
