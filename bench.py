@@ -373,24 +373,27 @@ def main():
     barrier()
     clocks = sampler.stop() if not args.no_clocks else None
 
-    # end to end through the public API: pinned host inputs -> device, step, results -> host
-    host_in = {
-        "q": q.cpu().pin_memory(), "gate": gate.cpu().pin_memory(), "logits": logits.cpu().pin_memory(),
-        "bt": bt.cpu().pin_memory(), "bounds": bounds.cpu().pin_memory(),
-        "drafts": drafts.cpu().pin_memory(), "kv_in": kv_in.cpu().pin_memory(),
-    }
-    dev_in = {kk: torch.empty_like(v, device=device) for kk, v in host_in.items()}
-    host_out = [torch.empty(n, dtype=torch.int32).pin_memory() for n in (R, R, R)]
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in host_out)
+    # end to end through the public API: the step's inputs from pinned host
+    # memory (two staged groups: attention inputs on the main stream, logits
+    # and drafts on the greedy verify's stream), the step, the results back
+    att = sv.StagedInputs(device, {"q_latent": (tuple(q.shape), q.dtype),
+                                   "gate": (tuple(gate.shape), gate.dtype),
+                                   "block_table": (tuple(bt.shape), bt.dtype),
+                                   "kv_bounds": (tuple(bounds.shape), bounds.dtype)})
+    ver = sv.StagedInputs(device, {"logits": (tuple(logits.shape), logits.dtype),
+                                   "draft_tokens": (tuple(drafts.shape), drafts.dtype),
+                                   "kv_lens_in": (tuple(kv_in.shape), kv_in.dtype)})
+    for grp, items in ((att, (("q_latent", q), ("gate", gate), ("block_table", bt), ("kv_bounds", bounds))),
+                       (ver, (("logits", logits), ("draft_tokens", drafts), ("kv_lens_in", kv_in)))):
+        for kk, v in items:
+            grp.host[kk].copy_(v.cpu())
+    host_out = torch.empty((3, R), dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for g in (att, ver) for t in g.host.values())
+    d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step():
-        for kk, v in host_in.items():
-            dev_in[kk].copy_(v, non_blocking=True)
-        res = step(dev_in["q"], kv, dev_in["bt"], dev_in["bounds"], dev_in["gate"], inp["softmax_scale"],
-                   dev_in["logits"], dev_in["drafts"], dev_in["kv_in"])
-        for h, dvc in zip(host_out, (res[3], res[4], res[5])):
-            h.copy_(dvc, non_blocking=True)
+        res = step.run_staged(att, ver, kv, inp["softmax_scale"])
+        host_out.copy_(res, non_blocking=True)
 
     for _ in range(3):
         e2e_step()

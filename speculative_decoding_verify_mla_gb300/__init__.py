@@ -25,4 +25,4 @@ from .binding import (  # noqa: F401
     spec_verify_sampled,
     status_string,
 )
-from .step import VerifyStep  # noqa: F401
+from .step import StagedInputs, VerifyStep  # noqa: F401

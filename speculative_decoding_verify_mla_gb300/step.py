@@ -33,9 +33,10 @@ class VerifyStep:
         self.greedy_ws = torch.zeros(B.greedy_workspace_bytes(T, V), dtype=torch.uint8,
                                      device=device)
         self.argmax = torch.empty(T, dtype=torch.int32, device=device)
-        self.accepted = torch.empty(R, dtype=torch.int32, device=device)
-        self.next_tokens = torch.empty(R, dtype=torch.int32, device=device)
-        self.kv_lens_out = torch.empty(R, dtype=torch.int32, device=device)
+        # the per-request results are rows of one [3, R] block, so a caller
+        # reads all of them back with a single device-to-host copy
+        self.results = torch.empty((3, R), dtype=torch.int32, device=device)
+        self.accepted, self.next_tokens, self.kv_lens_out = self.results[0], self.results[1], self.results[2]
         self.side = torch.cuda.Stream(device=device)
 
     def __call__(self, q_latent, kv_pages, block_table, kv_bounds, gate, softmax_scale,
@@ -53,6 +54,28 @@ class VerifyStep:
         main.wait_stream(self.side)
         return self.out, self.lse, self.argmax, self.accepted, self.next_tokens, self.kv_lens_out
 
+    def run_staged(self, att, ver, kv_pages, softmax_scale):
+        """The step fed from host memory through two StagedInputs: ``att``
+        (q_latent, gate, block_table, kv_bounds) is uploaded on the caller's
+        stream ahead of the attention, ``ver`` (logits, draft_tokens,
+        kv_lens_in) on the side stream ahead of the greedy verify, so the
+        logits copy overlaps the attention.  Returns the [3, R] results block
+        (accepted, next_tokens, kv_lens_out) on the caller's stream."""
+        main = torch.cuda.current_stream(self.device)
+        self.side.wait_stream(main)
+        att.upload()
+        with torch.cuda.stream(self.side):
+            ver.upload()
+            B.spec_verify_greedy(ver.dev["logits"], ver.dev["draft_tokens"], ver.dev["kv_lens_in"], self.k,
+                                 workspace=self.greedy_ws, argmax_ids=self.argmax,
+                                 accepted=self.accepted, next_tokens=self.next_tokens,
+                                 kv_lens_out=self.kv_lens_out)
+        B.mla_verify_decode(att.dev["q_latent"], kv_pages, att.dev["block_table"], att.dev["kv_bounds"],
+                            att.dev["gate"], self.k + 1, softmax_scale, num_splits=self.num_splits,
+                            workspace=self.attn_ws, out=self.out, lse=self.lse, status=self.status)
+        main.wait_stream(self.side)
+        return self.results
+
     @property
     def attention_launches(self) -> int:
         """Kernels one mla_verify_decode call enqueues: the balanced plan adds a
@@ -65,3 +88,32 @@ class VerifyStep:
     def launches_per_step(self) -> int:
         """Kernels one step enqueues: the attention call's kernels + greedy."""
         return self.attention_launches + 1
+
+
+class StagedInputs:
+    """A step's inputs in one pinned host buffer mirrored by one device buffer
+    (each tensor 256-byte aligned inside), so that a step moves all its
+    inputs with a single host-to-device copy instead of one per tensor.
+
+    ``specs`` maps a name to (shape, dtype).  Fill ``host[name]`` (pinned
+    views), call ``upload()`` on the step's stream, and pass ``dev[name]``
+    (device views) to the step."""
+
+    def __init__(self, device, specs: dict):
+        device = torch.device(device)
+        offsets, off = {}, 0
+        for name, (shape, dtype) in specs.items():
+            nbytes = int(torch.Size(shape).numel()) * torch.tensor([], dtype=dtype).element_size()
+            offsets[name] = (off, nbytes, tuple(shape), dtype)
+            off += (nbytes + 255) // 256 * 256
+        self.nbytes = off
+        self._host = torch.empty(off, dtype=torch.uint8).pin_memory()
+        self._dev = torch.empty(off, dtype=torch.uint8, device=device)
+        self.host, self.dev = {}, {}
+        for name, (o, n, shape, dtype) in offsets.items():
+            self.host[name] = self._host[o:o + n].view(dtype).view(shape)
+            self.dev[name] = self._dev[o:o + n].view(dtype).view(shape)
+
+    def upload(self):
+        """Host -> device copy of every input, asynchronous on the current stream."""
+        self._dev.copy_(self._host, non_blocking=True)
