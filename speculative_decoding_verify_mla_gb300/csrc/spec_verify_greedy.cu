@@ -6,14 +6,18 @@
 // request r accepts the longest prefix of its k drafts with d_j == a_{j-1};
 // next token a_n; kv_lens_out = kv_lens_in - (k - n).
 //
-// One launch.  The [T][V] fp32 logits are cut into chunks of C floats; each
-// CTA streams one chunk with coalesced 128-bit loads (eight in flight per
-// thread), reduces it to a 64-bit
-// key (order-preserving value bits << 32 | ~index, so the max key is the max
-// value at the lowest index) with warp shuffles, and parks the key in the
-// workspace.  The CTA that takes the last ticket reduces the keys per row,
-// writes the argmax ids, scans the drafts of every request and resets the
-// ticket to zero.  Nothing waits on another CTA.
+// One launch.  The [T][V] fp32 logits are cut into chunks of C floats (about
+// four CTAs per SM); each CTA streams one chunk with coalesced 128-bit loads
+// (eight in flight per thread), reduces it to a 64-bit key (order-preserving
+// value bits << 32 | ~index, so the max key is the max value at the lowest
+// index) and folds it into its row's key with a 64-bit atomicMax.  (Many
+// smaller CTAs stream a little faster but pay the per-CTA atomic, fence and
+// ticket latency once per wave: slower overall on GB300.)  The CTA that takes
+// the last ticket reads the row keys and the drafts in one round trip, marks
+// every mismatching draft with an atomicMax of (k - j) on its request's slot
+// (a zero slot means every draft matched), then writes accepted / next token /
+// trimmed kv_lens, and leaves the ticket and all slots zero again.  Nothing
+// waits on another CTA.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -59,8 +63,7 @@ __global__ void __launch_bounds__(kGreedyThreads)
                          const int32_t* __restrict__ kv_lens_in, int32_t* __restrict__ argmax_ids,
                          int32_t* __restrict__ accepted, int32_t* __restrict__ next_tokens,
                          int32_t* __restrict__ kv_lens_out, unsigned int* __restrict__ ticket,
-                         unsigned long long* __restrict__ keys, unsigned long long* row_key,
-                         int* n_acc) {
+                         unsigned long long* row_key, int* mis) {
   // Shared memory stays under 1 KB so that this kernel can share an SM with
   // the attention kernel (which leaves ~1.8 KB of the SM's shared memory).
   __shared__ unsigned long long s_warp[kGreedyThreads / 32];
@@ -118,84 +121,34 @@ __global__ void __launch_bounds__(kGreedyThreads)
     unsigned long long kk = tid < kGreedyThreads / 32 ? s_warp[tid] : 0ull;
     kk = warp_max_u64(kk);
     if (tid == 0) {
-      keys[(long long)t * nchunks + c] = kk;
+      atomicMax(row_key + t, kk);
       __threadfence();
-      const unsigned int prev = atomicAdd(ticket, 1u);
-      s_last = (prev == gridDim.x - 1);
+      s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1);
     }
   }
   __syncthreads();
   if (!s_last) return;
 
-  // ---- last CTA: per-row argmax, then acceptance and trim.  Every load of a
-  // phase is issued at once (block-strided, one element per thread) and the
-  // per-row / per-request results meet through L2 atomics on workspace slots,
-  // so the tail costs a few memory round trips instead of one per row.
+  // ---- last CTA: the row keys and the drafts in one round trip; a draft j
+  // that differs from its target's argmax raises its request's slot to k - j
+  // (the largest value marks the first mismatch); then accepted, next token
+  // and trim from the slots.  Every slot is left zero for the next call.
   // Global writes and atomics of this block are visible to all its threads
   // after __syncthreads; the reads go to L2 (.cg).
   __threadfence();
-  if (T <= 32) {
-    // small batch: one warp, lane t owns row t; the keys and the drafts are
-    // loaded at once, a ballot marks the mismatching drafts and a shuffle
-    // fetches each request's next token (two memory round trips)
-    if (tid < 32) {
-      const int t = tid;
-      const bool row = t < T;
-      const int rq = row ? t / (k + 1) : 0;
-      const int j = row ? t % (k + 1) : 0;
-      const int d = (row && j < k) ? __ldg(draft_tokens + (long long)rq * k + j) : -1;
-      unsigned long long best = 0ull;
-      if (row) {
-        const unsigned long long* kr = keys + (long long)t * nchunks;
-        int c2 = 0;
-        for (; c2 + 4 <= nchunks; c2 += 4) {
-          unsigned long long v[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) v[u] = __ldcg(kr + c2 + u);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) best = v[u] > best ? v[u] : best;
-        }
-        for (; c2 < nchunks; ++c2) {
-          const unsigned long long v = __ldcg(kr + c2);
-          best = v > best ? v : best;
-        }
-      }
-      const int a = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
-      if (row) argmax_ids[t] = a;
-      const unsigned mis = __ballot_sync(0xFFFFFFFFu, row && j < k && d != a);
-      int n = k;
-      if (t < R && k > 0) {
-        const unsigned seg = (mis >> (t * (k + 1))) & (k >= 32 ? 0xFFFFFFFFu : ((1u << k) - 1u));
-        n = seg ? __ffs(seg) - 1 : k;
-      }
-      const int nxt = __shfl_sync(0xFFFFFFFFu, a, t < R ? t * (k + 1) + n : 0);
-      if (t < R) {
-        accepted[t] = n;
-        next_tokens[t] = nxt;
-        kv_lens_out[t] = kv_lens_in[t] - (k - n);
-      }
-    }
-    if (tid == 0) *ticket = 0u;
-    return;
-  }
-  for (int tt = tid; tt < T; tt += kGreedyThreads) row_key[tt] = 0ull;
-  for (int r = tid; r < R; r += kGreedyThreads) n_acc[r] = k;
-  __syncthreads();
-  const long long nk = (long long)T * nchunks;
-  for (long long f = tid; f < nk; f += kGreedyThreads)
-    atomicMax(row_key + f / nchunks, __ldcg(keys + f));
-  __syncthreads();
-  for (int tt = tid; tt < T; tt += kGreedyThreads)
-    argmax_ids[tt] = (int32_t)(0xFFFFFFFFu - (uint32_t)(__ldcg(row_key + tt) & 0xFFFFFFFFull));
-  __syncthreads();
-  const long long nd = (long long)R * k;
-  for (long long f = tid; f < nd; f += kGreedyThreads) {
-    const int r = (int)(f / k), j = (int)(f % k);
-    if (__ldg(draft_tokens + f) != __ldcg(argmax_ids + r * (k + 1) + j)) atomicMin(n_acc + r, j);
+  for (int tt = tid; tt < T; tt += kGreedyThreads) {
+    const int rq = tt / (k + 1), j = tt - rq * (k + 1);
+    const int d = (j < k) ? __ldg(draft_tokens + (long long)rq * k + j) : 0;
+    const unsigned long long key = __ldcg(row_key + tt);
+    const int a = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+    argmax_ids[tt] = a;
+    row_key[tt] = 0ull;
+    if (j < k && d != a) atomicMax(mis + rq, k - j);
   }
   __syncthreads();
   for (int r = tid; r < R; r += kGreedyThreads) {
-    const int n = __ldcg(n_acc + r);
+    const int n = k - __ldcg(mis + r);
+    mis[r] = 0;
     accepted[r] = n;
     next_tokens[r] = __ldcg(argmax_ids + r * (k + 1) + n);
     kv_lens_out[r] = kv_lens_in[r] - (k - n);
@@ -203,8 +156,7 @@ __global__ void __launch_bounds__(kGreedyThreads)
   if (tid == 0) *ticket = 0u;  // leave the workspace zeroed for the next call
 }
 
-// Chunk length (floats) as a function of the problem only, so that the
-// workspace query and the launch agree.
+// Chunk length (floats) as a function of the problem only.
 int greedy_chunk(int T, int V) {
   const long long total = (long long)T * V;
   long long c = (total + 4 * 152 - 1) / (4 * 152);  // about four CTAs per SM
@@ -217,14 +169,11 @@ int greedy_chunk(int T, int V) {
 }  // namespace
 }  // namespace sv
 
-// Workspace: ticket header, then the chunk keys [T][nchunks], the per-row
-// keys [T] and the per-request accept counts [T >= R] of the tail.
+// Workspace: ticket header, then the row keys [T] and the per-request
+// mismatch slots [T >= R]; all zero at rest.
 extern "C" size_t sv_greedy_workspace_bytes(int T, int V) {
   if (T <= 0 || V <= 0) return sv::kGreedyHeader;
-  const int chunk = sv::greedy_chunk(T, V);
-  const long long nchunks = (V + (long long)chunk - 1) / chunk;
-  return sv::kGreedyHeader + (size_t)T * (size_t)nchunks * sizeof(unsigned long long) +
-         (size_t)T * sizeof(unsigned long long) + (size_t)T * sizeof(int);
+  return sv::kGreedyHeader + (size_t)T * sizeof(unsigned long long) + (size_t)T * sizeof(int);
 }
 
 extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R, int k,
@@ -251,14 +200,13 @@ extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R
   if (blocks > 0x7FFFFFFFll) return SV_ERR_SHAPE;
   const bool vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
   auto* ticket = reinterpret_cast<unsigned int*>(workspace);
-  auto* keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
-                                                     sv::kGreedyHeader);
-  auto* row_key = keys + (size_t)T * nchunks;
-  auto* n_acc = reinterpret_cast<int*>(row_key + T);
+  auto* row_key = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
+                                                        sv::kGreedyHeader);
+  auto* mis = reinterpret_cast<int*>(row_key + T);
   sv::greedy_verify_kernel<<<(unsigned)blocks, sv::kGreedyThreads, 0,
                              reinterpret_cast<cudaStream_t>(stream)>>>(
       logits, T, V, R, k, chunk, nchunks, vec4, draft_tokens, kv_lens_in, argmax_ids, accepted,
-      next_tokens, kv_lens_out, ticket, keys, row_key, n_acc);
+      next_tokens, kv_lens_out, ticket, row_key, mis);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_LAUNCH;
 }
 
@@ -269,8 +217,9 @@ extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R
 // a serving engine that has already handed (nearly) all of HBM to its own
 // KV-cache pool and forbids further cudaMalloc calls, or a plugin hosted by a
 // framework that owns the device allocator.  Such a caller cannot provide the
-// greedy workspace.  This entry point keeps that scratch (the ticket counter
-// and the per-chunk argmax keys) in a fixed file-scope device array instead.
+// greedy workspace.  This entry point keeps that scratch (the ticket counter,
+// the per-row argmax keys and the per-request mismatch slots) in a fixed
+// file-scope device array instead.
 //
 // Limits and sharing:
 //  * The array holds kNoAllocScratchBytes (512 KiB) on every GPU that loads
@@ -284,9 +233,9 @@ extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R
 //  * The first call on a device looks up the array's device address
 //    (cudaGetSymbolAddress) with that device current and caches it; make that
 //    first call before any stream capture begins.
-//  * The ticket counter must start at zero: each call clears it with a
-//    cudaMemsetAsync on the same stream before the kernel runs.  The keys need
-//    no initial value.
+//  * The counter, keys and slots must start at zero: each call clears the
+//    part it uses with a cudaMemsetAsync on the same stream before the kernel
+//    runs (every call also leaves them zero).
 // No cudaMalloc, cudaFree or other allocating routine is called.
 namespace sv {
 namespace {
@@ -329,8 +278,7 @@ extern "C" sv_status spec_verify_greedy_noalloc(const float* logits, int T, int 
   if (need > sv::kNoAllocScratchBytes) return SV_ERR_WORKSPACE;
   void* scratch = sv::noalloc_scratch_for_current_device();
   if (!scratch) return SV_ERR_DEVICE;
-  if (cudaMemsetAsync(scratch, 0, sv::kGreedyHeader, reinterpret_cast<cudaStream_t>(stream)) !=
-      cudaSuccess) {
+  if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return SV_ERR_LAUNCH;
   }

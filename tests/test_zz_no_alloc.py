@@ -68,7 +68,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
         pytest.skip("no CUDA device")
     import speculative_decoding_verify_mla_gb300 as sv
     lib = _lib()
-    T, V = 1 << 15, 1 << 20  # needs far more than 512 KiB of keys
+    T, V = 1 << 16, 1 << 20  # 12 bytes of scratch per token: more than 512 KiB
     assert sv.greedy_workspace_bytes(T, V) > 512 * 1024
     rc = lib.spec_verify_greedy_noalloc(4096, T, V, T, 0, None, 4096, 4096, 4096, 4096, 4096, None)
     assert rc == 4  # SV_ERR_WORKSPACE, nothing enqueued
