@@ -122,11 +122,12 @@ const char* sv_status_string(sv_status s);
  *                 sv_mla_verify_workspace_bytes(T, H, S) bytes (S = the
  *                 num_splits used, after resolving 0), 256-byte aligned; may
  *                 be NULL when S == 1.  With 2..SV_MAX_SPLITS uniform splits
- *                 it holds the split partials: part_o fp32 [S][T][H][512]
- *                 followed by part_lse fp32 [S][T][H] (lse of the split's KV
- *                 range, natural log, -inf for an empty range; part_o
- *                 normalised within the split, 0 for an empty range).  With
- *                 the balanced plan its layout is internal.
+ *                 it holds the split partials: part_o bf16 [S][T][H][512]
+ *                 (round to nearest even) followed by part_lse fp32
+ *                 [S][T][H] (lse of the split's KV range, natural log, -inf
+ *                 for an empty range; part_o normalised within the split, 0
+ *                 for an empty range).  With the balanced plan its layout is
+ *                 internal.
  *   workspace_bytes  its size in bytes.
  *   out           bf16 [T][H][512] (round to nearest even).
  *   lse           fp32 [T][H], natural log of the ungated scaled scores.

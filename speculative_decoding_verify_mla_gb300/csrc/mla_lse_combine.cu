@@ -10,9 +10,12 @@
 // row cannot poison the merge with 0 * NaN.
 //
 // HBM-bound: one warp per half row (256 of the 512 columns); each lane owns
-// two float4 of every split (coalesced 512-byte warp accesses), the loads of
-// eight splits are in flight before their FMAs, and the gate and the output
-// move as 8-byte bf16x4 accesses.
+// columns 4 lane + 128 j .. +3 (j = 0, 1) of every split, so a warp access is
+// contiguous (512 bytes for fp32 partials, 256 for bf16); the loads of the
+// first splits are in flight with the split weights and later ones eight at
+// a time, and the gate and the output move as 8-byte bf16x4 accesses.  Two
+// partial formats: fp32 (the public entry point) and bf16 (what the
+// attention kernel writes for its own splits).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -25,12 +28,47 @@ namespace {
 
 constexpr int kCombineThreads = 256;
 
+// Partial formats: the raw value a lane loads for four columns, and its
+// conversion to fp32 (bf16 -> fp32 is exact).
+template <bool kBf16>
+struct Partial;
+template <>
+struct Partial<false> {
+  using Elem = float;
+  using Raw = float4;
+  static constexpr int kFirst = 12;
+  __device__ static Raw load(const Elem* p) { return ld_dep_f4_stream(reinterpret_cast<const float4*>(p)); }
+  __device__ static Raw zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ static float4 f4(Raw r) { return r; }
+};
+template <>
+struct Partial<true> {
+  using Elem = __nv_bfloat16;
+  using Raw = uint2;
+  static constexpr int kFirst = 16;
+  __device__ static Raw load(const Elem* p) { return ld_dep_u2_stream(p); }
+  __device__ static Raw zero() { return make_uint2(0u, 0u); }
+  __device__ static float4 f4(Raw r) {
+    return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xFFFF0000u),
+                       __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xFFFF0000u));
+  }
+};
+
+__device__ __forceinline__ void fma4(float4& acc, float w, float4 v) {
+  acc.x = fmaf(w, v.x, acc.x);
+  acc.y = fmaf(w, v.y, acc.y);
+  acc.z = fmaf(w, v.z, acc.z);
+  acc.w = fmaf(w, v.w, acc.w);
+}
+
 // Partial addressing.  Uniform splits: split s of row `row` is slot s, row
 // `row` of a [S][rows] table.  Balanced plan (plan_splits != NULL): request r
 // = row / Mq owns slots plan_base[r] .. + plan_splits[r] - 1 of a [slots][Mq]
 // table, and a request with one piece was finished by the attention kernel.
+template <bool kBf16>
 __global__ void __launch_bounds__(kCombineThreads)
-    lse_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+    lse_combine_kernel(const typename Partial<kBf16>::Elem* __restrict__ part_o,
+                       const float* __restrict__ part_lse,
                        int S_uniform, long long rows, const __nv_bfloat16* __restrict__ gate,
                        __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out,
                        const int* plan_splits, const int* plan_base, int Mq, int gate_dim) {
@@ -70,18 +108,17 @@ __global__ void __launch_bounds__(kCombineThreads)
   // partials of the first kFirst splits are loaded in the same round trip
   // (every split's partial is written, as zeros when its range is empty, so
   // they can be read before the weights are known).
-  constexpr int kFirst = 12;
+  using P = Partial<kBf16>;
+  constexpr int kFirst = P::kFirst;
   float l0 = -INFINITY, l1 = -INFINITY;
   if (lane < S) l0 = ld_dep_f32(part_lse + (slot0 + lane) * slot_rows + rin);
   if (lane + 32 < S) l1 = ld_dep_f32(part_lse + (slot0 + lane + 32) * slot_rows + rin);
-  float4 v0[kFirst][2];
+  typename P::Raw v0[kFirst][2];
 #pragma unroll
   for (int u = 0; u < kFirst; ++u) {
-    const float* src = part_o + ((slot0 + min(u, S - 1)) * slot_rows + rin) * 512 + col0;
+    const auto* src = part_o + ((slot0 + min(u, S - 1)) * slot_rows + rin) * 512 + col0;
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
-      v0[u][j] = (u < S) ? ld_dep_f4_stream(reinterpret_cast<const float4*>(src + 128 * j))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < 2; ++j) v0[u][j] = (u < S) ? P::load(src + 128 * j) : P::zero();
   }
   float m = fmaxf(l0, l1);
 #pragma unroll
@@ -102,36 +139,24 @@ __global__ void __launch_bounds__(kCombineThreads)
       const float ws = (u < S) ? __shfl_sync(0xFFFFFFFFu, w0, u) * inv_z : 0.f;
       if (ws == 0.f) continue;  // an empty split's values are never used (0 * NaN stays out)
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        acc[j].x = fmaf(ws, v0[u][j].x, acc[j].x);
-        acc[j].y = fmaf(ws, v0[u][j].y, acc[j].y);
-        acc[j].z = fmaf(ws, v0[u][j].z, acc[j].z);
-        acc[j].w = fmaf(ws, v0[u][j].w, acc[j].w);
-      }
+      for (int j = 0; j < 2; ++j) fma4(acc[j], ws, P::f4(v0[u][j]));
     }
     // further splits, eight per round: all their loads in flight before any FMA
     for (int s0 = kFirst; s0 < S; s0 += 8) {
-      float4 v[8][2];
+      typename P::Raw v[8][2];
       float ws[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int s = s0 + u;
         ws[u] = (s < S) ? __shfl_sync(0xFFFFFFFFu, s < 32 ? w0 : w1, s & 31) * inv_z : 0.f;
-        const float* src = part_o + ((slot0 + min(s, S - 1)) * slot_rows + rin) * 512 + col0;
+        const auto* src = part_o + ((slot0 + min(s, S - 1)) * slot_rows + rin) * 512 + col0;
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-          v[u][j] = (ws[u] != 0.f) ? ld_dep_f4_stream(reinterpret_cast<const float4*>(src + 128 * j))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < 2; ++j) v[u][j] = (ws[u] != 0.f) ? P::load(src + 128 * j) : P::zero();
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          acc[j].x = fmaf(ws[u], v[u][j].x, acc[j].x);
-          acc[j].y = fmaf(ws[u], v[u][j].y, acc[j].y);
-          acc[j].z = fmaf(ws[u], v[u][j].z, acc[j].z);
-          acc[j].w = fmaf(ws[u], v[u][j].w, acc[j].w);
-        }
+        for (int j = 0; j < 2; ++j) fma4(acc[j], ws[u], P::f4(v[u][j]));
       }
     }
   }
@@ -154,10 +179,12 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 }  // namespace
 
-// Internal launcher shared with mla_verify_decode (no argument checks).
-cudaError_t launch_lse_combine(const float* part_o, const float* part_lse, int S, long long rows,
-                               const void* gate, void* out, float* lse, cudaStream_t stream,
-                               const int* plan_splits, const int* plan_base, int Mq, int gate_dim) {
+// Internal launcher shared with mla_verify_decode (no argument checks);
+// part_o is fp32, or bf16 when bf16_partials.
+cudaError_t launch_lse_combine(const void* part_o, bool bf16_partials, const float* part_lse, int S,
+                               long long rows, const void* gate, void* out, float* lse,
+                               cudaStream_t stream, const int* plan_splits, const int* plan_base,
+                               int Mq, int gate_dim) {
   if (rows == 0) return cudaSuccess;
   const long long blocks = (2 * rows + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
   // programmatic dependent launch: the grid may start while the previous
@@ -172,10 +199,15 @@ cudaError_t launch_lse_combine(const float* part_o, const float* part_lse, int S
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, lse_combine_kernel, part_o, part_lse, S, rows,
-                                           static_cast<const __nv_bfloat16*>(gate),
-                                           static_cast<__nv_bfloat16*>(out), lse, plan_splits,
-                                           plan_base, Mq, gate_dim);
+  const auto* g = static_cast<const __nv_bfloat16*>(gate);
+  auto* o = static_cast<__nv_bfloat16*>(out);
+  const cudaError_t e =
+      bf16_partials
+          ? cudaLaunchKernelEx(&cfg, lse_combine_kernel<true>,
+                               static_cast<const __nv_bfloat16*>(part_o), part_lse, S, rows, g, o,
+                               lse, plan_splits, plan_base, Mq, gate_dim)
+          : cudaLaunchKernelEx(&cfg, lse_combine_kernel<false>, static_cast<const float*>(part_o),
+                               part_lse, S, rows, g, o, lse, plan_splits, plan_base, Mq, gate_dim);
   if (e != cudaSuccess) cudaGetLastError();
   return e;
 }
@@ -195,7 +227,7 @@ extern "C" sv_status mla_lse_combine(const float* part_o, const float* part_lse,
       (reinterpret_cast<uintptr_t>(gate) & 7u) || (reinterpret_cast<uintptr_t>(out) & 7u) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return SV_ERR_ALIGN;
-  return sv::launch_lse_combine(part_o, part_lse, S, rows, gate, out, lse,
+  return sv::launch_lse_combine(part_o, false, part_lse, S, rows, gate, out, lse,
                                 reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr,
                                 1, SV_LATENT_DIM) == cudaSuccess
              ? SV_OK

@@ -53,9 +53,10 @@
 
 namespace sv {
 
-cudaError_t launch_lse_combine(const float* part_o, const float* part_lse, int S, long long rows,
-                               const void* gate, void* out, float* lse, cudaStream_t stream,
-                               const int* plan_splits, const int* plan_base, int Mq, int gate_dim);
+cudaError_t launch_lse_combine(const void* part_o, bool bf16_partials, const float* part_lse, int S,
+                               long long rows, const void* gate, void* out, float* lse,
+                               cudaStream_t stream, const int* plan_splits, const int* plan_base,
+                               int Mq, int gate_dim);
 
 namespace {
 
@@ -98,9 +99,9 @@ struct KernelShape {
 };
 static_assert(KernelShape<false>::kSmemBytes <= 232448 && KernelShape<true>::kSmemBytes <= 232448,
               "shared memory budget");
-static_assert(KernelShape<false>::kOffBar - KernelShape<false>::kOffOwn >= 8 * kQBoxBytes &&
-                  KernelShape<true>::kOffBar - KernelShape<true>::kOffOwn >= 8 * kQBoxBytes,
-              "the epilogue stages a 128 x 256 fp32 tile over the idle KV buffers");
+static_assert(KernelShape<false>::kOffBar - KernelShape<false>::kOffOwn >= 4 * kQBoxBytes &&
+                  KernelShape<true>::kOffBar - KernelShape<true>::kOffOwn >= 4 * kQBoxBytes,
+              "the epilogue stages a 128 x 256 bf16 tile over the idle KV buffers");
 
 struct VerifyParams {
   const __nv_bfloat16* q;
@@ -109,7 +110,7 @@ struct VerifyParams {
   const __nv_bfloat16* gate;
   __nv_bfloat16* out;
   float* lse;
-  float* part_o;
+  __nv_bfloat16* part_o;  // split partials o/l, bf16 [slot][rows][512]
   float* part_lse;
   int32_t* status;
   long long rows_total;  // T * H
@@ -551,8 +552,10 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       mbar_arrive(p_full(sb));
     }
 
-    // ---- epilogue: O/l (gated bf16, or fp32 partial) staged swizzled in SMEM,
-    // then written with TMA tensor stores (coalesced; rows past M are dropped)
+    // ---- epilogue: O/l as bf16 (gated when this unit finishes its rows, else
+    // the split partial), one 64-column box at a time: the box is staged
+    // swizzled in the idle KV ring and the leader starts its TMA tensor store
+    // (rows past M are dropped) while the next box is staged
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // a dependent merge may launch
     if (ok && ntiles > 0)
       ok = warp_wait(pv_done((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
@@ -565,86 +568,70 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
     uint8_t* const stage = sptr + kOffOwn;
     const uint32_t row_off = (uint32_t)i * 128u;
     const uint32_t swz = (uint32_t)(i & 7);
-    if (fused_gate) {
-      // head-wise gate: one sigmoid per row; elementwise: the staged gate tile
-      const bool row_gate = (p.gate_dim == 1);
-      const float g_row = (row_gate && valid) ? fast_sigmoid(__bfloat162float(p.gate[row_g])) : 0.f;
-      const bool gate_ok = !row_gate && warp_wait(gate_full, 0, abort_flag, p.status);
-      const uint8_t* const gs = sptr + kOffQ;
+    // gate: head-wise, one sigmoid per row; elementwise, the staged gate tile;
+    // a partial is not gated (the merge gates)
+    const bool row_gate = fused_gate && p.gate_dim == 1;
+    const bool elem_gate = fused_gate && p.gate_dim != 1;
+    float g_row = 1.f;
+    if (row_gate) g_row = valid ? fast_sigmoid(__bfloat162float(p.gate[row_g])) : 0.f;
+    const bool gate_ok = elem_gate && warp_wait(gate_full, 0, abort_flag, p.status);
+    const uint8_t* const gs = sptr + kOffQ;
+    const uint32_t st0 = sbase + kOffOwn;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t v[32];
-        if (have_o) {
-          tmem_ld32(tmem + lane_off + kTmemO + 32u * c, v);
-          tmem_wait_ld();
-        } else {
+    for (int bx = 0; bx < 4; ++bx) {
+      uint32_t va[32], vb[32];  // columns 64 bx .. +31 and 64 bx + 32 .. +63
+      if (have_o) {
+        tmem_ld32(tmem + lane_off + kTmemO + 64u * bx, va);
+        tmem_ld32(tmem + lane_off + kTmemO + 64u * bx + 32u, vb);
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) v[u] = 0u;
-        }
-        // columns 32c .. 32c+31 of this half: box c/2, 16-byte chunks (c%2)*4 + u
+        for (int u = 0; u < 32; ++u) va[u] = vb[u] = 0u;
+      }
+      auto v = [&](int c) { return __uint_as_float(c < 32 ? va[c] : vb[c - 32]); };
+      // 16-byte chunk u of the row holds columns 64 bx + 8u .. +7
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t off = (uint32_t)(c >> 1) * kQBoxBytes + row_off +
-                               (((uint32_t)((c & 1) * 4 + u) ^ swz) << 4);
-          uint4 graw = gate_ok ? *reinterpret_cast<const uint4*>(gs + off) : make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t off = (uint32_t)bx * kQBoxBytes + row_off + (((uint32_t)u ^ swz) << 4);
+        uint32_t ow[4];
+        if (elem_gate) {
+          const uint4 graw = gate_ok ? *reinterpret_cast<const uint4*>(gs + off) : make_uint4(0u, 0u, 0u, 0u);
           const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
-          uint32_t ow[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
-            const float s0 = row_gate ? g_row : fast_sigmoid(gf.x);
-            const float s1 = row_gate ? g_row : fast_sigmoid(gf.y);
-            const float o0 = __uint_as_float(v[8 * u + 2 * e]) * inv_l * s0;
-            const float o1 = __uint_as_float(v[8 * u + 2 * e + 1]) * inv_l * s1;
-            ow[e] = pack_bf16x2(o0, o1);
+            ow[e] = pack_bf16x2(v(8 * u + 2 * e) * inv_l * fast_sigmoid(gf.x),
+                                v(8 * u + 2 * e + 1) * inv_l * fast_sigmoid(gf.y));
           }
-          *reinterpret_cast<uint4*>(stage + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-        }
-      }
-      if (valid && half == 0) p.lse[row_g] = lse_v;
-    } else {
-      // fp32: 32 columns per 128-byte box row; columns 32c .. 32c+31 are box c
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t v[32];
-        if (have_o) {
-          tmem_ld32(tmem + lane_off + kTmemO + 32u * c, v);
-          tmem_wait_ld();
         } else {
+          const float f = inv_l * g_row;
 #pragma unroll
-          for (int u = 0; u < 32; ++u) v[u] = 0u;
+          for (int e = 0; e < 4; ++e)
+            ow[e] = pack_bf16x2(v(8 * u + 2 * e) * f, v(8 * u + 2 * e + 1) * f);
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t off = (uint32_t)c * kQBoxBytes + row_off + (((uint32_t)u ^ swz) << 4);
-          *reinterpret_cast<float4*>(stage + off) =
-              make_float4(__uint_as_float(v[4 * u]) * inv_l, __uint_as_float(v[4 * u + 1]) * inv_l,
-                          __uint_as_float(v[4 * u + 2]) * inv_l, __uint_as_float(v[4 * u + 3]) * inv_l);
-        }
+        *reinterpret_cast<uint4*>(stage + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
       }
-      if (valid && half == 0) {
+      fence_proxy_async_smem();
+      named_bar_sync(kEpilogueBarId, 128);
+      if (leader) {
+        if (fused_gate)
+          tma_store_3d(&tmap_out, st0 + bx * kQBoxBytes, half * kDHalf + bx * 64, m_tile * kMTile, r);
+        else
+          tma_store_4d(&tmap_part, st0 + bx * kQBoxBytes, half * kDHalf + bx * 64, m_tile * kMTile,
+                       p.units ? 0 : r, p.units ? slot : s_idx);
+        tma_store_commit();
+      }
+    }
+    if (valid && half == 0) {
+      if (fused_gate) {
+        p.lse[row_g] = lse_v;
+      } else {
         const long long w = p.units ? slot : s_idx;
         const long long z = p.units ? 0 : r;
         p.part_lse[w * p.part_w_stride + z * Mq + f] = lse_v;
       }
     }
-    fence_proxy_async_smem();
-    named_bar_sync(kEpilogueBarId, 128);
-    if (leader) {
-      const uint32_t st0 = sbase + kOffOwn;
-      if (fused_gate) {
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-          tma_store_3d(&tmap_out, st0 + b * kQBoxBytes, half * kDHalf + b * 64, m_tile * kMTile, r);
-      } else {
-#pragma unroll
-        for (int b = 0; b < 8; ++b)
-          tma_store_4d(&tmap_part, st0 + b * kQBoxBytes, half * kDHalf + b * 32, m_tile * kMTile,
-                       p.units ? 0 : r, p.units ? slot : s_idx);
-      }
-      tma_store_commit();
-      tma_store_wait_read();  // SMEM stays valid until the stores have read it
-    }
+    if (leader) tma_store_wait_read();  // SMEM stays valid until the stores have read it
     __syncwarp();
   }
 
@@ -950,7 +937,7 @@ PlanLayout plan_layout(int R, int Mq, int n_mt, int sms) {
   L.base = L.splits + align256((size_t)R * 4);
   L.units = L.base + align256((size_t)R * 4);
   L.part_o = L.units + align256((size_t)L.units_max * 16);
-  L.part_lse = L.part_o + align256((size_t)L.slots_max * Mq * kD * 4);
+  L.part_lse = L.part_o + align256((size_t)L.slots_max * Mq * kD * 2);
   L.total = L.part_lse + align256((size_t)L.slots_max * Mq * 4);
   return L;
 }
@@ -961,7 +948,7 @@ size_t plan_workspace_bound(long long T, long long H, int sms) {
   const long long units_max = 2ll * sms + 2 * (rows / 128 + T);
   const long long slot_rows = 128ll * sms + 2 * rows;
   return 256 + 2 * align256((size_t)T * 4) + align256((size_t)units_max * 16) +
-         align256((size_t)slot_rows * kD * 4) + align256((size_t)slot_rows * 4) + 1024;
+         align256((size_t)slot_rows * kD * 2) + align256((size_t)slot_rows * 4) + 1024;
 }
 
 }  // namespace
@@ -986,7 +973,7 @@ extern "C" size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits) {
   if (num_splits == SV_SPLITS_BALANCED) return sv::plan_workspace_bound(T, H, sv::current_sm_count());
   if (num_splits <= 1) return 0;
   const size_t rows = (size_t)T * (size_t)H;
-  const size_t o_bytes = (size_t)num_splits * rows * sv::kD * sizeof(float);
+  const size_t o_bytes = (size_t)num_splits * rows * sv::kD * sizeof(__nv_bfloat16);
   return o_bytes + (size_t)num_splits * rows * sizeof(float);
 }
 
@@ -1027,7 +1014,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   const bool balanced = (S == SV_SPLITS_BALANCED);
   const long long Mq_ll = (long long)H * q_per_req;
   const int n_mt = (int)((Mq_ll + kMTile - 1) / kMTile);
-  float* part_o = nullptr;
+  __nv_bfloat16* part_o = nullptr;
   float* part_lse = nullptr;
   PlanLayout PL{};
   char* plan_base_ptr = nullptr;
@@ -1039,14 +1026,14 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
         workspace_bytes < sv_mla_verify_workspace_bytes((int)T, H, SV_SPLITS_BALANCED))
       return SV_ERR_WORKSPACE;
     plan_base_ptr = static_cast<char*>(workspace);
-    part_o = reinterpret_cast<float*>(plan_base_ptr + PL.part_o);
+    part_o = reinterpret_cast<__nv_bfloat16*>(plan_base_ptr + PL.part_o);
     part_lse = reinterpret_cast<float*>(plan_base_ptr + PL.part_lse);
   } else if (S > 1) {
     if (!workspace) return SV_ERR_WORKSPACE;
     if (misaligned(workspace, 256)) return SV_ERR_ALIGN;
     if (workspace_bytes < sv_mla_verify_workspace_bytes((int)T, H, S)) return SV_ERR_WORKSPACE;
-    part_o = static_cast<float*>(workspace);
-    part_lse = part_o + (size_t)S * T * H * kD;
+    part_o = static_cast<__nv_bfloat16*>(workspace);
+    part_lse = reinterpret_cast<float*>(part_o + (size_t)S * T * H * kD);
   }
   if (!get_encode_fn()) return SV_ERR_DEVICE;
   const long long Mq = (long long)H * q_per_req;
@@ -1067,13 +1054,13 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
       return SV_ERR_ALIGN;
     if (balanced) {
       const cuuint64_t part_dims[4] = {(cuuint64_t)kD, (cuuint64_t)Mq, 1, (cuuint64_t)PL.slots_max};
-      const cuuint32_t part_box[4] = {32, (cuuint32_t)kMTile, 1, 1};
-      if (!encode_map(&tmap_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, part_o, 4, part_dims, part_box))
+      const cuuint32_t part_box[4] = {64, (cuuint32_t)kMTile, 1, 1};
+      if (!encode_map(&tmap_part, bf16, 2, part_o, 4, part_dims, part_box))
         return SV_ERR_ALIGN;
     } else if (S > 1) {
       const cuuint64_t part_dims[4] = {(cuuint64_t)kD, (cuuint64_t)Mq, (cuuint64_t)R, (cuuint64_t)S};
-      const cuuint32_t part_box[4] = {32, (cuuint32_t)kMTile, 1, 1};
-      if (!encode_map(&tmap_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, part_o, 4, part_dims, part_box))
+      const cuuint32_t part_box[4] = {64, (cuuint32_t)kMTile, 1, 1};
+      if (!encode_map(&tmap_part, bf16, 2, part_o, 4, part_dims, part_box))
         return SV_ERR_ALIGN;
     } else {
       tmap_part = tmap_out;  // unused with one split
@@ -1119,7 +1106,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
     kernel<<<(unsigned)ctas, threads, smem, st>>>(tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part,
                                                   prm);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_LAUNCH;
-    if (S > 1 && launch_lse_combine(part_o, part_lse, S, T * H, gate, out, lse, st, nullptr,
+    if (S > 1 && launch_lse_combine(part_o, true, part_lse, S, T * H, gate, out, lse, st, nullptr,
                                     nullptr, 1, gate_dim) != cudaSuccess)
       return SV_ERR_LAUNCH;
     return SV_OK;
@@ -1153,7 +1140,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
     cudaGetLastError();
     return SV_ERR_LAUNCH;
   }
-  if (launch_lse_combine(part_o, part_lse, 0, T * H, gate, out, lse, st, splits, pbase,
+  if (launch_lse_combine(part_o, true, part_lse, 0, T * H, gate, out, lse, st, splits, pbase,
                          (int)Mq_ll, gate_dim) != cudaSuccess)
     return SV_ERR_LAUNCH;
   return SV_OK;

@@ -108,6 +108,11 @@ __device__ __forceinline__ float4 ld_dep_f4_stream(const float4* p) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ uint2 ld_dep_u2_stream(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.cs.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ int4 ld_dep_i4(const void* p) {
   int4 v;
   asm volatile("ld.global.cg.v4.s32 {%0, %1, %2, %3}, [%4];"

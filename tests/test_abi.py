@@ -53,7 +53,7 @@ def test_status_strings(lib):
 def test_workspace_queries(lib):
     from speculative_decoding_verify_mla_gb300 import attention_workspace_bytes, greedy_workspace_bytes
     assert attention_workspace_bytes(8, 64, 1) == 0
-    assert attention_workspace_bytes(8, 64, 3) == 3 * 8 * 64 * (512 + 1) * 4
+    assert attention_workspace_bytes(8, 64, 3) == 3 * 8 * 64 * (512 * 2 + 4)  # bf16 part_o + fp32 part_lse
     assert greedy_workspace_bytes(8, 163840) >= 256 + 8 * 8
     assert greedy_workspace_bytes(0, 10) == 256
 

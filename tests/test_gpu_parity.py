@@ -199,9 +199,9 @@ def test_attention_partials_layout(sv):
     sv.mla_verify_decode(d["q"], d["kv"], d["block_table"], d["kv_bounds"], d["gate"], inp["k"] + 1,
                          inp["softmax_scale"], num_splits=S, workspace=ws)
     torch.cuda.synchronize()
-    wsf = ws.view(torch.float32)
-    part_o = wsf[:S * T * H * 512].view(S, T, H, 512)
-    part_lse = wsf[S * T * H * 512:S * T * H * 513].view(S, T, H)
+    n_o = S * T * H * 512
+    part_o = ws[:2 * n_o].view(torch.bfloat16).view(S, T, H, 512)
+    part_lse = ws[2 * n_o:2 * n_o + 4 * S * T * H].view(torch.float32).view(S, T, H)
     k1 = inp["k"] + 1
     edges = []
     for r in range(inp["R"]):
