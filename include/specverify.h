@@ -181,9 +181,13 @@ sv_status mla_verify_decode_gated(const void* q_latent, const void* kv_pages, in
  * so this is the "next" variant): kv_pages_e4m3 holds OCP FP8 E4M3 codes
  * [num_pages][64][512] (1 byte each, 16-byte aligned) and the cached latent
  * row is code value * kv_scale (one scale for the pool, finite and > 0).
- * The kernel converts each tile to bf16 in shared memory (exact) and folds
- * kv_scale into the score scale and the output.  Everything else as
- * mla_verify_decode_gated; the workspace query is the same.
+ * The tensor-core products of this variant take f16 operands: each KV tile
+ * is converted to f16 in shared memory (exact), q_latent is rounded to f16
+ * (exact for |q| in [2^-14, 65504]; larger magnitudes overflow, so q must
+ * stay below 65504) and the softmax weights P are f16 (bf16 in the bf16
+ * variant); kv_scale is folded into the score scale and the output.
+ * Everything else as mla_verify_decode_gated; the workspace query is the
+ * same.
  * ---------------------------------------------------------------------- */
 sv_status mla_verify_decode_kv8(const void* q_latent, const void* kv_pages_e4m3, float kv_scale,
                                 int num_pages, int page_size, const int32_t* block_table, int R,

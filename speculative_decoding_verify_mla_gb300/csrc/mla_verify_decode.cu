@@ -76,17 +76,20 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kF8TileBytes = 64 * kD;  // one fp8 KV tile: 64 rows x 512 e4m3 codes
 
 // Two variants of the kernel.  bf16 KV: the TMA producer fills the bf16 KV
-// rings.  fp8 KV: four converter warps (warps 6..9) read each e4m3 tile from
-// global memory one tile ahead into registers (coalesced 16-byte loads) and
-// write it as bf16 into the same swizzled ring slots the MMAs read (e4m3 ->
-// bf16 is exact); the producer then only loads the query half.
+// rings and every MMA takes bf16 operands.  fp8 KV: the MMAs take f16
+// operands (e4m3 -> f16 is one exact conversion per two codes); four
+// converter warps (warps 6..9) read each e4m3 tile from global memory one
+// tile ahead into registers (coalesced 16-byte loads) and write it as f16
+// into the same swizzled ring slots, and also write the other query half as
+// f16 into shared memory; the softmax warps put their query half into TMEM
+// as f16 and write P as f16.
 template <bool kF8>
 struct KernelShape {
   static constexpr int kOwnStages = 3;
   static constexpr int kOthStages = 2;
   static constexpr int kF8Stages = 0;
   static constexpr int kThreads = kF8 ? 320 : 192;
-  static constexpr int kNumBars = 19;
+  static constexpr int kNumBars = 20;
   static constexpr int kFullCount = kF8 ? 128 : 1;  // arrivals completing a KV ring slot
   // shared memory map (offsets from the 1024-aligned base)
   static constexpr int kOffQ = 0;
@@ -126,15 +129,11 @@ struct VerifyParams {
   const uint8_t* kv8;       // fp8 KV: the e4m3 page pool [pages][64][512]
 };
 
-// Two e4m3 codes (low byte first) -> two bf16 (low half first); exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+// Two e4m3 codes (low byte first) -> two f16 (low half first); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   uint32_t h2;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
-  float lo, hi;
-  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h2));
-  return pack_bf16x2(lo, hi);
+  return h2;
 }
 
 __device__ __forceinline__ int load_bound(const VerifyParams& p, int tok) {
@@ -193,6 +192,7 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
   const uint32_t q_ready = bar0 + 8u * 16;  // Q own half in TMEM + Q other half in SMEM
   const uint32_t drain_bar = bar0 + 8u * 17;
   const uint32_t gate_full = bar0 + 8u * 18;  // gate tile staged in the Q region
+  const uint32_t q_tma = bar0 + 8u * 19;      // fp8 KV: bf16 query half landed (converted in place)
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sptr + kOffBar + 8 * kNumBars);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(sptr + kOffBar + 8 * kNumBars + 4);
 
@@ -259,9 +259,12 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       mbar_init(p_full(b), 128);
       mbar_init(pv_done(b), 1);
     }
-    mbar_init(q_ready, 128 + 1);  // 128 softmax threads (TMEM half) + the producer (TMA half)
+    // 128 softmax threads (TMEM half) + the other half: the producer's TMA
+    // (bf16) or the 128 converter threads (fp8 KV, f16 query)
+    mbar_init(q_ready, kF8 ? 128 + 128 : 128 + 1);
     mbar_init(drain_bar, 1);
     mbar_init(gate_full, 1);
+    mbar_init(q_tma, 1);
     *abort_flag = 0;
     fence_mbar_init_cluster();
   }
@@ -296,14 +299,16 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ntiles > 0) {
-      tma_prefetch_desc(&tmap_kv);
-      // the other latent half of this unit's 128 query rows (A of the SMEM score GEMM)
-      mbar_arrive_expect_tx(q_ready, kQHalfBytes);
+      // the other latent half of this unit's 128 query rows (A of the SMEM
+      // score GEMM); fp8 KV: bf16, converted to f16 in place by the converters
+      const uint32_t q_bar = kF8 ? q_tma : q_ready;
+      mbar_arrive_expect_tx(q_bar, kQHalfBytes);
 #pragma unroll
       for (int b = 0; b < 4; ++b)
-        tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_ready, (1 - half) * kDHalf + b * 64,
+        tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_bar, (1 - half) * kDHalf + b * 64,
                     m_tile * kMTile, r);
       if constexpr (!kF8) {
+      tma_prefetch_desc(&tmap_kv);
       int last_own[kOwnStages];
       int last_oth[kOthStages];
       for (int s = 0; s < kOwnStages; ++s) last_own[s] = -1;
@@ -343,16 +348,16 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       for (int s = 0; s < kOthStages; ++s)
         if (last_oth[s] >= 0) drain_wait(oth_full(s), last_oth[s] & 1);
       } else {
-        // fp8 KV: the converter warps fill the KV rings; only the query copy
-        // has to land before teardown
-        drain_wait(q_ready, 0);
+        // fp8 KV: the converter warps fill the KV rings; the query copy has
+        // to land before teardown
+        drain_wait(q_tma, 0);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
+    constexpr uint32_t idesc_s = kF8 ? idesc_f16_f32(128, 64, false, false) : idesc_bf16_f32(128, 64, false, false);
+    constexpr uint32_t idesc_pv = kF8 ? idesc_f16_f32(128, 256, false, true) : idesc_bf16_f32(128, 256, false, true);
     bool ok = ntiles > 0 && warp_wait(q_ready, 0, abort_flag, p.status);
     bool issued = false;
     auto issue_pv = [&](int i) -> bool {
@@ -463,6 +468,10 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
           v[4 * u + 2] = qv[8 * c + u].z;
           v[4 * u + 3] = qv[8 * c + u].w;
         }
+        if constexpr (kF8) {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) v[u] = bf16x2_to_f16x2(v[u]);
+        }
         tmem_st32(tmem + lane_off + kTmemQ + 32u * c, v);
       }
       tmem_wait_st();
@@ -543,7 +552,7 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
         const float p0 = fast_exp2(x[2 * c] - msub);
         const float p1 = fast_exp2(x[2 * c + 1] - msub);
         psum += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+        pk[c] = kF8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
       }
       l_sum += psum;
       tmem_st32(tmem + lane_off + kTmemS + 64u * sb, pk);  // P over the consumed scores
@@ -638,10 +647,12 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
   if constexpr (kF8) {
     if (warp >= 6) {
       // ---------------------------------------------------------- fp8 converters
-      // 128 threads: tile it's 64 x 512 codes are loaded into registers while
-      // tile it-1 is converted (thread ct holds 16 chunks of 16 codes: row
-      // 4k + ct/32, columns 16 (ct%32) .. +15), then written as bf16 into the
-      // own / other ring slots of tile it, swizzled like a TMA box.
+      // 128 threads.  First the other latent half of the unit's query rows
+      // (TMA-loaded as bf16) is converted to f16 in shared memory.  Then the
+      // KV: tile it's 64 x 512 codes are loaded into
+      // registers while tile it-1 is converted (thread ct holds 16 chunks of 16
+      // codes: row 4k + ct/32, columns 16 (ct%32) .. +15), then written as f16
+      // into the own / other ring slots of tile it, swizzled like a TMA box.
       const int ct = threadIdx.x - 192;
       const int32_t* bt_row = p.block_table + (long long)r * p.max_pages + lo;
       uint4 buf[16];
@@ -655,8 +666,24 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 16; ++k) buf[k] = __ldcs(base + (k * 128 + ct));
       };
-      if (ntiles > 0) load_tile(0);
       bool ok = true;
+      if (ntiles > 0) {
+        load_tile(0);
+        // the bf16 query half -> f16 in place (elementwise, so the swizzle
+        // is kept); rows past M arrived as zeros
+        ok = mbar_wait<false>(q_tma, 0, abort_flag, p.status);
+        if (ok) {
+          uint4* const qs = reinterpret_cast<uint4*>(sptr + kOffQ);
+#pragma unroll 4
+          for (int u = 0; u < kQHalfBytes / 16 / 128; ++u) {
+            const uint4 w = qs[u * 128 + ct];
+            qs[u * 128 + ct] = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y),
+                                          bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+          }
+          fence_proxy_async_smem();  // the tensor cores read what the threads wrote
+          mbar_arrive(q_ready);
+        }
+      }
       for (int it = 0; ok && it < ntiles; ++it) {
         const int so = it % kOwnStages, ro = it / kOwnStages;
         const int sx = it % kOthStages, rx = it / kOthStages;
@@ -675,14 +702,14 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
           const int b = (col & 255) >> 6;
           const int j0 = (col & 63) >> 3;  // 16-byte chunks j0, j0+1 of the 128-byte row
           uint4 w0, w1;
-          w0.x = e4m3x2_to_bf16x2(v.x);
-          w0.y = e4m3x2_to_bf16x2(v.x >> 16);
-          w0.z = e4m3x2_to_bf16x2(v.y);
-          w0.w = e4m3x2_to_bf16x2(v.y >> 16);
-          w1.x = e4m3x2_to_bf16x2(v.z);
-          w1.y = e4m3x2_to_bf16x2(v.z >> 16);
-          w1.z = e4m3x2_to_bf16x2(v.w);
-          w1.w = e4m3x2_to_bf16x2(v.w >> 16);
+          w0.x = e4m3x2_to_f16x2(v.x);
+          w0.y = e4m3x2_to_f16x2(v.x >> 16);
+          w0.z = e4m3x2_to_f16x2(v.y);
+          w0.w = e4m3x2_to_f16x2(v.y >> 16);
+          w1.x = e4m3x2_to_f16x2(v.z);
+          w1.y = e4m3x2_to_f16x2(v.z >> 16);
+          w1.z = e4m3x2_to_f16x2(v.w);
+          w1.w = e4m3x2_to_f16x2(v.w >> 16);
           uint8_t* const rb = ring + b * kBoxBytes + row * 128;
           *reinterpret_cast<uint4*>(rb + (((uint32_t)j0 ^ (uint32_t)(row & 7)) << 4)) = w0;
           *reinterpret_cast<uint4*>(rb + (((uint32_t)(j0 + 1) ^ (uint32_t)(row & 7)) << 4)) = w1;
