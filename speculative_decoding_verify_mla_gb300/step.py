@@ -12,7 +12,11 @@ class VerifyStep:
     The two parts are independent (the greedy verify reads the target logits,
     not the attention output), so the greedy kernel runs on a side stream
     forked from and joined back into the caller's stream: the step costs
-    about max(attention, greedy) instead of their sum.  Output buffers and
+    about max(attention, greedy) instead of their sum.  The attention is
+    enqueued first so that its grid (one CTA per SM, nearly all of the SM's
+    shared memory) is placed before the greedy CTAs fill the SMs; a CUDA
+    graph captured from the step keeps that order (captured greedy-first,
+    the C = 32 step replayed in 118.9 us instead of 104.9 us on GB300).  Output buffers and
     both workspaces are allocated once (torch) and reused, so a step enqueues
     exactly the library's kernels and nothing else."""
 
@@ -43,14 +47,14 @@ class VerifyStep:
                  logits, draft_tokens, kv_lens_in):
         main = torch.cuda.current_stream(self.device)
         self.side.wait_stream(main)
+        B.mla_verify_decode(q_latent, kv_pages, block_table, kv_bounds, gate, self.k + 1,
+                            softmax_scale, num_splits=self.num_splits, workspace=self.attn_ws,
+                            out=self.out, lse=self.lse, status=self.status)
         with torch.cuda.stream(self.side):
             B.spec_verify_greedy(logits, draft_tokens, kv_lens_in, self.k,
                                  workspace=self.greedy_ws, argmax_ids=self.argmax,
                                  accepted=self.accepted, next_tokens=self.next_tokens,
                                  kv_lens_out=self.kv_lens_out)
-        B.mla_verify_decode(q_latent, kv_pages, block_table, kv_bounds, gate, self.k + 1,
-                            softmax_scale, num_splits=self.num_splits, workspace=self.attn_ws,
-                            out=self.out, lse=self.lse, status=self.status)
         main.wait_stream(self.side)
         return self.out, self.lse, self.argmax, self.accepted, self.next_tokens, self.kv_lens_out
 
@@ -63,16 +67,17 @@ class VerifyStep:
         (accepted, next_tokens, kv_lens_out) on the caller's stream."""
         main = torch.cuda.current_stream(self.device)
         self.side.wait_stream(main)
-        att.upload()
+        att.upload()  # the small attention inputs first, so the attention can start
         with torch.cuda.stream(self.side):
-            ver.upload()
+            ver.upload()  # the logits copy overlaps the attention
+        B.mla_verify_decode(att.dev["q_latent"], kv_pages, att.dev["block_table"], att.dev["kv_bounds"],
+                            att.dev["gate"], self.k + 1, softmax_scale, num_splits=self.num_splits,
+                            workspace=self.attn_ws, out=self.out, lse=self.lse, status=self.status)
+        with torch.cuda.stream(self.side):
             B.spec_verify_greedy(ver.dev["logits"], ver.dev["draft_tokens"], ver.dev["kv_lens_in"], self.k,
                                  workspace=self.greedy_ws, argmax_ids=self.argmax,
                                  accepted=self.accepted, next_tokens=self.next_tokens,
                                  kv_lens_out=self.kv_lens_out)
-        B.mla_verify_decode(att.dev["q_latent"], kv_pages, att.dev["block_table"], att.dev["kv_bounds"],
-                            att.dev["gate"], self.k + 1, softmax_scale, num_splits=self.num_splits,
-                            workspace=self.attn_ws, out=self.out, lse=self.lse, status=self.status)
         main.wait_stream(self.side)
         return self.results
 
