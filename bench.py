@@ -370,6 +370,17 @@ def main():
     w_uv = torch.from_numpy(w_np.view(np.int16)).view(torch.bfloat16).to(device)
     out_v = torch.empty((T, H, 128), dtype=torch.bfloat16, device=device)
     wuv_ms = timed(lambda: sv.mla_wuv_project(step.out, w_uv, out_v=out_v), args.steps)
+    # the LSE merge + gate on its own (the public entry point, fp32 partials
+    # read from HBM after the flush), over the step's split count (4 when the
+    # step does not split)
+    s_comb = step.num_splits if step.num_splits > 1 else 4
+    g_comb = torch.Generator(device=device).manual_seed(rank + 11)
+    part_o = torch.randn((s_comb, T, H, 512), generator=g_comb, device=device)
+    part_lse = torch.randn((s_comb, T, H), generator=g_comb, device=device)
+    comb_out, comb_lse = torch.empty_like(step.out), torch.empty_like(step.lse)
+    comb_ms = timed(lambda: sv.mla_lse_combine(part_o, part_lse, gate, out=comb_out, lse=comb_lse), args.steps)
+    comb_bytes = s_comb * T * H * (2048 + 4) + T * H * (1024 + 1024 + 4)
+    del part_o, part_lse
     barrier()
     clocks = sampler.stop() if not args.no_clocks else None
 
@@ -410,6 +421,7 @@ def main():
     sampled_mean = agg(sampled_ms)
     wuv_mean = agg(wuv_ms)
     kv8_mean = agg(kv8_ms)
+    comb_mean = agg(comb_ms)
     graph_mean = agg(graph_ms) if graph_ms else None
     if rank != 0:
         if world > 1:
@@ -469,6 +481,10 @@ def main():
         "attention_kv8_tflops": attn_flops / (kv8_mean * 1e-3) / 1e12,
         "wuv_project_us": wuv_mean * 1000.0,
         "wuv_project_tflops": 2.0 * T * H * 128 * 512 / (wuv_mean * 1e-3) / 1e12,
+        "combine_us": comb_mean * 1000.0,
+        "combine_splits": s_comb,
+        "combine_gbps": comb_bytes / (comb_mean * 1e-3) / 1e9,
+        "combine_hbm_frac": comb_bytes / (comb_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
         "steps_per_s_all_gpus": replica_throughput(step_mean, world),
         "roofline": roof,
         "cpu_baseline": base,
@@ -476,7 +492,7 @@ def main():
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * step.launches_per_step,
         "gpu_launches_all_timed_loops": args.steps * (3 * step.launches_per_step + step.attention_launches
-                                                       + 1 + 1 + 2 + 1 + step.attention_launches),
+                                                       + 1 + 1 + 2 + 1 + step.attention_launches + 1),
         "clocks": clocks,
         "status_word": int(step.status.item()),
     }

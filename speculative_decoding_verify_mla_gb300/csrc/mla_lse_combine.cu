@@ -36,7 +36,7 @@ template <>
 struct Partial<false> {
   using Elem = float;
   using Raw = float4;
-  static constexpr int kFirst = 12;
+  static constexpr int kMaxFirst = 12;
   __device__ static Raw load(const Elem* p) { return ld_dep_f4_stream(reinterpret_cast<const float4*>(p)); }
   __device__ static Raw zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
   __device__ static float4 f4(Raw r) { return r; }
@@ -45,7 +45,7 @@ template <>
 struct Partial<true> {
   using Elem = __nv_bfloat16;
   using Raw = uint2;
-  static constexpr int kFirst = 16;
+  static constexpr int kMaxFirst = 16;
   __device__ static Raw load(const Elem* p) { return ld_dep_u2_stream(p); }
   __device__ static Raw zero() { return make_uint2(0u, 0u); }
   __device__ static float4 f4(Raw r) {
@@ -65,7 +65,9 @@ __device__ __forceinline__ void fma4(float4& acc, float w, float4 v) {
 // `row` of a [S][rows] table.  Balanced plan (plan_splits != NULL): request r
 // = row / Mq owns slots plan_base[r] .. + plan_splits[r] - 1 of a [slots][Mq]
 // table, and a request with one piece was finished by the attention kernel.
-template <bool kBf16>
+// kFirst: splits whose partials are loaded with the weights (chosen from S at
+// launch, so that few splits keep few registers and many warps resident).
+template <bool kBf16, int kFirst>
 __global__ void __launch_bounds__(kCombineThreads)
     lse_combine_kernel(const typename Partial<kBf16>::Elem* __restrict__ part_o,
                        const float* __restrict__ part_lse,
@@ -109,7 +111,6 @@ __global__ void __launch_bounds__(kCombineThreads)
   // (every split's partial is written, as zeros when its range is empty, so
   // they can be read before the weights are known).
   using P = Partial<kBf16>;
-  constexpr int kFirst = P::kFirst;
   float l0 = -INFINITY, l1 = -INFINITY;
   if (lane < S) l0 = ld_dep_f32(part_lse + (slot0 + lane) * slot_rows + rin);
   if (lane + 32 < S) l1 = ld_dep_f32(part_lse + (slot0 + lane + 32) * slot_rows + rin);
@@ -141,12 +142,13 @@ __global__ void __launch_bounds__(kCombineThreads)
 #pragma unroll
       for (int j = 0; j < 2; ++j) fma4(acc[j], ws, P::f4(v0[u][j]));
     }
-    // further splits, eight per round: all their loads in flight before any FMA
-    for (int s0 = kFirst; s0 < S; s0 += 8) {
-      typename P::Raw v[8][2];
-      float ws[8];
+    // further splits, kRound per round: all their loads in flight before any FMA
+    constexpr int kRound = kFirst < 8 ? kFirst : 8;
+    for (int s0 = kFirst; s0 < S; s0 += kRound) {
+      typename P::Raw v[kRound][2];
+      float ws[kRound];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kRound; ++u) {
         const int s = s0 + u;
         ws[u] = (s < S) ? __shfl_sync(0xFFFFFFFFu, s < 32 ? w0 : w1, s & 31) * inv_z : 0.f;
         const auto* src = part_o + ((slot0 + min(s, S - 1)) * slot_rows + rin) * 512 + col0;
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(kCombineThreads)
         for (int j = 0; j < 2; ++j) v[u][j] = (ws[u] != 0.f) ? P::load(src + 128 * j) : P::zero();
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kRound; ++u) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) fma4(acc[j], ws[u], P::f4(v[u][j]));
       }
@@ -201,13 +203,24 @@ cudaError_t launch_lse_combine(const void* part_o, bool bf16_partials, const flo
   cfg.numAttrs = 1;
   const auto* g = static_cast<const __nv_bfloat16*>(gate);
   auto* o = static_cast<__nv_bfloat16*>(out);
-  const cudaError_t e =
-      bf16_partials
-          ? cudaLaunchKernelEx(&cfg, lse_combine_kernel<true>,
-                               static_cast<const __nv_bfloat16*>(part_o), part_lse, S, rows, g, o,
-                               lse, plan_splits, plan_base, Mq, gate_dim)
-          : cudaLaunchKernelEx(&cfg, lse_combine_kernel<false>, static_cast<const float*>(part_o),
-                               part_lse, S, rows, g, o, lse, plan_splits, plan_base, Mq, gate_dim);
+  // the balanced plan's split counts are only known on the device: widest bucket
+  const int s_max = plan_splits ? SV_MAX_SPLITS : S;
+  auto launch = [&](auto kernel, const auto* po) {
+    return cudaLaunchKernelEx(&cfg, kernel, po, part_lse, S, rows, g, o, lse, plan_splits, plan_base,
+                              Mq, gate_dim);
+  };
+  cudaError_t e;
+  if (bf16_partials) {
+    const auto* po = static_cast<const __nv_bfloat16*>(part_o);
+    e = s_max <= 4 ? launch(lse_combine_kernel<true, 4>, po)
+        : s_max <= 8 ? launch(lse_combine_kernel<true, 8>, po)
+                     : launch(lse_combine_kernel<true, Partial<true>::kMaxFirst>, po);
+  } else {
+    const auto* po = static_cast<const float*>(part_o);
+    e = s_max <= 4 ? launch(lse_combine_kernel<false, 4>, po)
+        : s_max <= 8 ? launch(lse_combine_kernel<false, 8>, po)
+                     : launch(lse_combine_kernel<false, Partial<false>::kMaxFirst>, po);
+  }
   if (e != cudaSuccess) cudaGetLastError();
   return e;
 }

@@ -416,6 +416,26 @@ def test_balanced_plan_head_shapes(sv, H, k, lens):
     check_attention(out, lse, ref_o, ref_l, label=f"balanced H={H} k={k}")
 
 
+@pytest.mark.parametrize("S", [1, 4, 5, 8, 9, 13, 21, 40])
+def test_combine_split_counts(sv, S):
+    """Every split-count bucket of the merge kernel (the first 4 / 8 / 12
+    splits loaded with the weights, later ones in rounds), with uneven and
+    empty ranges."""
+    cfg = small_config("c0", R=2, k=3, H=16, kv_lens=(150, 260))
+    inp = make_inputs(cfg, seed=20 + S)
+    edges = []
+    for L in (150, 260):
+        cuts = sorted(np.random.default_rng(S + L).integers(0, L + 1, size=S - 1).tolist())
+        edges.append([0] + cuts + [L])
+    po, pl = oracle.ref_attention_partials(inp["q_bits"], inp["kv_bits"], inp["block_table"], inp["kv_bounds"], 4,
+                                           inp["softmax_scale"], edges)
+    ref_o, ref_l = oracle.ref_lse_combine(po, pl, inp["gate_bits"])
+    out, lse = sv.mla_lse_combine(torch.from_numpy(po.astype(np.float32)).to(DEV),
+                                  torch.from_numpy(pl.astype(np.float32)).to(DEV), bf16_tensor(inp["gate_bits"], DEV))
+    torch.cuda.synchronize()
+    check_attention(out, lse, ref_o, ref_l, label=f"combine S={S}")
+
+
 def test_combine_ignores_values_of_empty_splits(sv):
     """A split with lse = -inf has weight 0; whatever its o holds (NaN here)
     must not reach the output (0 * NaN would poison the row)."""
