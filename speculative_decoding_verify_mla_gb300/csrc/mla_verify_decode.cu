@@ -358,6 +358,7 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_s = kF8 ? idesc_f16_f32(128, 64, false, false) : idesc_bf16_f32(128, 64, false, false);
     constexpr uint32_t idesc_pv = kF8 ? idesc_f16_f32(128, 256, false, true) : idesc_bf16_f32(128, 256, false, true);
+    const uint64_t q_desc = sdesc_sw128(q_s, 16, 1024);  // A of the other-half score MMAs
     bool ok = ntiles > 0 && warp_wait(q_ready, 0, abort_flag, p.status);
     bool issued = false;
     auto issue_pv = [&](int i) -> bool {
@@ -367,13 +368,16 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       tc_fence_after();
       if (lane == 0) {
         const uint32_t a = tmem + kTmemS + 64u * sb;
-        const uint32_t sa = own0 + so * kHalfTileBytes;
+        // descriptors differ only in the 14-bit start-address field, which
+        // never carries (shared addresses < 256 KB): one add per MMA
+        const uint64_t pv_desc0 = sdesc_sw128(own0 + so * kHalfTileBytes, kBoxBytes, 1024);
+        const uint32_t pv_lo = (uint32_t)pv_desc0, pv_hi = (uint32_t)(pv_desc0 >> 32);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           // B = V tile (own half), MN-major: N = 256 latent columns in four
           // 64-wide boxes (LBO = box stride), K = 16 KV rows per step (SBO = 8-row stride).
-          const uint64_t bd = sdesc_sw128(sa + kk * 16 * 128, kBoxBytes, 1024);
-          mma_ts(tmem + kTmemO, a + 8u * kk, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_w(tmem + kTmemO, a + 8u * kk, pv_lo + (uint32_t)((kk * 16 * 128) >> 4), pv_hi, idesc_pv,
+                   (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(own_empty(so));
         mma_commit(pv_done(sb));
@@ -411,21 +415,23 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       }
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t ko = own0 + so * kHalfTileBytes;
-        const uint32_t kx = oth0 + sx * kHalfTileBytes;
+        const uint64_t ko_desc = sdesc_sw128(own0 + so * kHalfTileBytes, 16, 1024);
+        const uint64_t kx_desc = sdesc_sw128(oth0 + sx * kHalfTileBytes, 16, 1024);
+        const uint32_t ko_lo = (uint32_t)ko_desc, kx_lo = (uint32_t)kx_desc;
+        const uint32_t k_hi = (uint32_t)(ko_desc >> 32);  // the same for every K-major operand
+        const uint32_t q_lo = (uint32_t)q_desc;
         const uint32_t d = tmem + kTmemS + 64u * sb;
         // B = K tile, K-major, 128-byte swizzle: step 16 latent columns (32
         // bytes) inside a box, next box every 4 steps.
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(ko + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
-          mma_ts(d, tmem + kTmemQ + 8u * kk, bd, idesc_s, kk > 0 ? 1u : 0u);
+          mma_ts_w(d, tmem + kTmemQ + 8u * kk, ko_lo + (uint32_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4),
+                   k_hi, idesc_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(q_s + (kk >> 2) * kQBoxBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(kx + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
-          mma_ss(d, ad, bd, idesc_s, 1u);
+          mma_ss_w(d, q_lo + (uint32_t)(((kk >> 2) * kQBoxBytes + (kk & 3) * 32) >> 4), k_hi,
+                   kx_lo + (uint32_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4), k_hi, idesc_s, 1u);
         }
         mma_commit(s_full(sb));
         mma_commit(oth_empty(sx));
