@@ -35,8 +35,11 @@
 //    2-stage ring that is released as soon as the score MMA completes.  Pool
 //    slack beyond the tile's largest bound is zeroed in SMEM before use
 //    (0 * NaN safety).
-//  * Epilogue.  One split: normalise, gate (prefetched with cp.async), bf16
-//    out + lse.  Several splits: fp32 partials (o/l, lse) for the LSE merge.
+//  * Epilogue.  One split: normalise, gate (the gate tile TMA-loaded into the
+//    query region after the last score MMA), bf16 out + lse.  Several
+//    splits: bf16 o/l and fp32 lse partials for the LSE merge.  The output
+//    leaves in four 64-column boxes by TMA stores, each started as soon as
+//    its box is staged.
 //  * Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 softmax and
 //    epilogue.  Every wait is bounded; nothing traps.
 #include <cuda.h>
