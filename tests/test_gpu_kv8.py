@@ -87,3 +87,41 @@ def test_kv8_equals_bf16_on_exact_pool(sv):
     fin = torch.isfinite(l16)
     assert torch.equal(torch.isfinite(l8), fin)
     assert torch.allclose(l8[fin], l16[fin], rtol=0, atol=1e-4)
+
+
+def test_kv8_c4_sampled(sv):
+    """Full-size long-context workload over the fp8 pool (balanced plan); the
+    oracle checks every zero-bound token and two whole straddling groups, each
+    against its own request's dequantised pages only."""
+    inp = make_inputs("c4", seed=0)
+    codes, scale = fp8_kv_pool(inp)
+    d = device_inputs(inp, DEV)
+    kv8 = torch.from_numpy(codes).to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse = sv.mla_verify_decode(d["q"], kv8, d["block_table"], d["kv_bounds"], d["gate"], inp["k"] + 1,
+                                    inp["softmax_scale"], status=status, kv_scale=scale)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    del kv8
+    k1 = inp["k"] + 1
+    L = inp["kv_lens_in"]
+    straddle = [r for r in range(inp["R"]) if 1 <= L[r] % 64 <= inp["k"]][:2]
+    toks = sorted(set(inp["zero_bound_tokens"].tolist()) | {r * k1 + t for r in straddle for t in range(k1)})
+    ref_o = np.zeros((len(toks), inp["H"], 512))
+    ref_l = np.zeros((len(toks), inp["H"]))
+    lut = oracle.e4m3_bits_to_f64(np.arange(256, dtype=np.uint8)) * scale  # the oracle's decode of every code
+    pools = {}
+    for n, t in enumerate(toks):
+        r = t // k1
+        n_pages = -(-int(inp["kv_bounds"][t]) // 64)
+        if n_pages == 0:  # a zero bound reads no row: any one-page pool will do
+            pool, n_pages = np.zeros((1, 64, 512)), 1
+        else:
+            if r not in pools:  # this request's pages, in order
+                pools[r] = lut[codes[inp["block_table"][r, :-(-int(L[r]) // 64)]]]
+            pool = pools[r]
+        o1, l1 = oracle.ref_verify_attention(inp["q_bits"][t:t + 1], pool, np.arange(n_pages)[None, :],
+                                             inp["kv_bounds"][t:t + 1], inp["gate_bits"][t:t + 1], 1,
+                                             inp["softmax_scale"])
+        ref_o[n], ref_l[n] = o1[0], l1[0]
+    check_attention(out, lse, ref_o, ref_l, rows=np.array(toks), label="kv8 c4 sampled")
