@@ -40,8 +40,14 @@
 //    splits: bf16 o/l and fp32 lse partials for the LSE merge.  The output
 //    leaves in four 64-column boxes by TMA stores, each started as soon as
 //    its box is staged.
+//  * Work units.  Uniform splits decode the unit from blockIdx; the balanced
+//    plan (a one-CTA plan kernel, this grid its programmatic dependent) hands
+//    each CTA a unit of a list ordered longest first.
+//  * MMA issue.  One thread issues every MMA, so each ring slot's descriptor
+//    is built once and a K step adds a constant to its low word.
 //  * Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 softmax and
-//    epilogue.  Every wait is bounded; nothing traps.
+//    epilogue; the fp8-KV instance adds converter warps 6-9.  Every wait is
+//    bounded; nothing traps.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
