@@ -66,6 +66,23 @@ def test_greedy_configs_bit_exact(sv, name):
         assert np.array_equal(gkv.cpu().numpy(), kv)
 
 
+@pytest.mark.parametrize("R,k,V,p", [(3, 40, 3000, 0.97), (1, 63, 163840, 0.99), (200, 1, 5000, 0.5)])
+def test_greedy_group_sizes(sv, R, k, V, p):
+    """Long verify groups (k + 1 > 32, drafts matching with high probability
+    so that long prefixes are accepted) and many short ones, against the oracle."""
+    cfg = small_config("c0", R=R, k=k, H=1, vocab=V, draft_p=p, kv_lens=None, kv_len_range=(k + 2, k + 300))
+    inp = make_inputs(cfg, seed=R + k)
+    d = device_inputs(inp, DEV)
+    a, n, nxt, kv = oracle.ref_greedy_verify(inp["logits"], inp["draft_tokens"], inp["kv_lens_in"], k)
+    ga, gn, gnxt, gkv = sv.spec_verify_greedy(d["logits"], d["draft_tokens"], d["kv_lens_in"], k)
+    torch.cuda.synchronize()
+    assert np.array_equal(ga.cpu().numpy(), a)
+    assert np.array_equal(gn.cpu().numpy(), n)
+    assert np.array_equal(gnxt.cpu().numpy(), nxt)
+    assert np.array_equal(gkv.cpu().numpy(), kv)
+    assert n.min() >= 0 and n.max() <= k
+
+
 def _greedy_case(sv, logits, drafts, kv_in, k):
     lt = torch.from_numpy(np.ascontiguousarray(logits, dtype=np.float32)).to(DEV)
     dt = torch.from_numpy(np.ascontiguousarray(np.asarray(drafts, dtype=np.int32).reshape(len(kv_in), k))).to(DEV)
@@ -245,7 +262,8 @@ def test_nan_in_pool_slack_does_not_leak(sv):
         check_attention(out, lse, ref_o, ref_l, label=f"nan slack, splits={splits}")
 
 
-@pytest.mark.parametrize("H,k,lens", [(96, 1, (300, 129)), (1, 0, (65, 1, 640)), (8, 19, (500,)), (64, 7, (64,))])
+@pytest.mark.parametrize("H,k,lens", [(96, 1, (300, 129)), (1, 0, (65, 1, 640)), (8, 19, (500,)), (64, 7, (64,)),
+                                      (3, 40, (700, 300)), (8, 35, (900,))])
 def test_attention_head_and_group_shapes(sv, H, k, lens):
     cfg = small_config("c0", R=len(lens), k=k, H=H, kv_lens=lens, shuffled=True, vocab=64)
     inp = make_inputs(cfg, seed=6)
@@ -407,7 +425,8 @@ def test_balanced_plan_zero_bounds_and_nan_slack(sv):
     check_attention(out, lse, ref_o, ref_l, label="balanced zero bounds + nan slack")
 
 
-@pytest.mark.parametrize("H,k,lens", [(96, 1, (300, 129, 3000)), (1, 0, (65, 1, 640)), (8, 19, (500, 64))])
+@pytest.mark.parametrize("H,k,lens", [(96, 1, (300, 129, 3000)), (1, 0, (65, 1, 640)), (8, 19, (500, 64)),
+                                      (3, 40, (700, 4200))])
 def test_balanced_plan_head_shapes(sv, H, k, lens):
     cfg = small_config("c0", R=len(lens), k=k, H=H, kv_lens=lens, shuffled=True, vocab=64)
     inp = make_inputs(cfg, seed=23)
