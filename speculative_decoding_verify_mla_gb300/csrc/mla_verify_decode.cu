@@ -23,6 +23,9 @@
 //    M=128, N=64) plus Q[:, other] K[:, other]^T with A from swizzled SMEM.
 //    Both halves of a unit therefore compute the same scores (1.5x the
 //    algorithmic tensor work), but no CTA ever waits on another SM.
+//  * Query.  The producer TMA-loads the CTA's query half into the idle
+//    other-half KV ring and the other half into its SMEM region; the softmax
+//    warps move their rows of the first into TMEM and release the ring.
 //  * Softmax.  One thread per query row: scale, per-token bound mask, running
 //    max with a lazy rescale (O is rescaled in TMEM only when the max grows by
 //    more than 2^8), exp2, bf16 P written back into the score buffer in TMEM.
@@ -98,7 +101,7 @@ struct KernelShape {
   static constexpr int kOthStages = 2;
   static constexpr int kF8Stages = 0;
   static constexpr int kThreads = kF8 ? 320 : 192;
-  static constexpr int kNumBars = 20;
+  static constexpr int kNumBars = 22;
   static constexpr int kFullCount = kF8 ? 128 : 1;  // arrivals completing a KV ring slot
   // shared memory map (offsets from the 1024-aligned base)
   static constexpr int kOffQ = 0;
@@ -202,6 +205,10 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * 17;
   const uint32_t gate_full = bar0 + 8u * 18;  // gate tile staged in the Q region
   const uint32_t q_tma = bar0 + 8u * 19;      // fp8 KV: bf16 query half landed (converted in place)
+  // this CTA's query half, TMA-staged in the idle other-half ring, landed /
+  // copied into TMEM (the ring slots may take KV tiles)
+  const uint32_t q_own_full = bar0 + 8u * 20;
+  const uint32_t q_own_free = bar0 + 8u * 21;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sptr + kOffBar + 8 * kNumBars);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(sptr + kOffBar + 8 * kNumBars + 4);
 
@@ -243,15 +250,6 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
     if (lane == 0) prefetch_l2(p.kv_bounds + r * p.q_per_req);
     if (lane == 1) prefetch_l2(p.kv_bounds + r * p.q_per_req + p.q_per_req - 1);
   }
-  // softmax warps: start fetching this CTA's half of their query row now, so
-  // the load overlaps the set-up below (row i of the tile <-> TMEM lane i)
-  uint4 qv[32];
-  if (warp >= 2) {
-    const int f0 = m_tile * kMTile + (warp & 3) * 32 + lane;
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((long long)r * Mq + f0) * kD + half * kDHalf);
-#pragma unroll
-    for (int u = 0; u < 32; ++u) qv[u] = (f0 < Mq) ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kOwnStages; ++s) {
@@ -274,6 +272,8 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
     mbar_init(drain_bar, 1);
     mbar_init(gate_full, 1);
     mbar_init(q_tma, 1);
+    mbar_init(q_own_full, 1);
+    mbar_init(q_own_free, 128);
     *abort_flag = 0;
     fence_mbar_init_cluster();
   }
@@ -308,6 +308,13 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ntiles > 0) {
+      // this CTA's latent half of the unit's 128 query rows, staged in the
+      // idle other-half ring for the softmax warps to move into TMEM (one
+      // bulk copy instead of 64 KB of per-thread loads)
+      mbar_arrive_expect_tx(q_own_full, kQHalfBytes);
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        tma_load_3d(oth0 + b * kQBoxBytes, &tmap_q, q_own_full, half * kDHalf + b * 64, m_tile * kMTile, r);
       // the other latent half of this unit's 128 query rows (A of the SMEM
       // score GEMM); fp8 KV: bf16, converted to f16 in place by the converters
       const uint32_t q_bar = kF8 ? q_tma : q_ready;
@@ -339,9 +346,11 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
           tma_load_2d(own0 + so * kHalfTileBytes + b * kBoxBytes, &tmap_kv, own_full(so),
                       half * kDHalf + b * 64, page * kTileN);
         last_own[so] = ro;
-        // other half: scores only
+        // other half: scores only (its ring holds the staged query half until
+        // the softmax warps have moved it into TMEM)
         const int sx = it % kOthStages;
         const int rx = it / kOthStages;
+        if (it == 0 && !mbar_wait<false>(q_own_free, 0, abort_flag, p.status)) break;
         if (rx > 0 && !mbar_wait<false>(oth_empty(sx), (rx - 1) & 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(oth_full(sx), kHalfTileBytes);
 #pragma unroll
@@ -351,14 +360,16 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
         last_oth[sx] = rx;
       }
       // every copy this CTA started has landed before teardown
+      drain_wait(q_own_full, 0);
       drain_wait(q_ready, 0);
       for (int s = 0; s < kOwnStages; ++s)
         if (last_own[s] >= 0) drain_wait(own_full(s), last_own[s] & 1);
       for (int s = 0; s < kOthStages; ++s)
         if (last_oth[s] >= 0) drain_wait(oth_full(s), last_oth[s] & 1);
       } else {
-        // fp8 KV: the converter warps fill the KV rings; the query copy has
+        // fp8 KV: the converter warps fill the KV rings; the query copies have
         // to land before teardown
+        drain_wait(q_own_full, 0);
         drain_wait(q_tma, 0);
       }
     }
@@ -471,17 +482,21 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
     const int b_i = valid ? load_bound(p, r * p.q_per_req + t_loc) : 0;
     const bool fused_gate = fused;
 
-    if (ntiles > 0) {
-      // this CTA's half of the query row -> TMEM (bf16 pairs per 32-bit column)
+    if (ntiles > 0 && warp_wait(q_own_full, 0, abort_flag, p.status)) {
+      // this CTA's half of the query row, staged by TMA (row i of box c at
+      // c * 16 KB + 128 i, 16-byte chunks swizzled by i mod 8) -> TMEM (bf16
+      // pairs per 32-bit column); rows past M arrived as zeros
+      const uint8_t* const qrow = sptr + kOffOth + i * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          v[4 * u + 0] = qv[8 * c + u].x;
-          v[4 * u + 1] = qv[8 * c + u].y;
-          v[4 * u + 2] = qv[8 * c + u].z;
-          v[4 * u + 3] = qv[8 * c + u].w;
+          const uint4 w = *reinterpret_cast<const uint4*>(qrow + c * kQBoxBytes + (((uint32_t)u ^ (uint32_t)(i & 7)) << 4));
+          v[4 * u + 0] = w.x;
+          v[4 * u + 1] = w.y;
+          v[4 * u + 2] = w.z;
+          v[4 * u + 3] = w.w;
         }
         if constexpr (kF8) {
 #pragma unroll
@@ -492,6 +507,7 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(q_ready);
+      mbar_arrive(q_own_free);  // the staging slots may take KV tiles
     }
     // Stage the gate tile (128 rows x 256 columns) into the Q region once no
     // score GEMM will read it again.
@@ -698,6 +714,9 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
           fence_proxy_async_smem();  // the tensor cores read what the threads wrote
           mbar_arrive(q_ready);
         }
+        // the other-half ring holds the staged query half until the softmax
+        // warps have moved it into TMEM
+        if (ok) ok = mbar_wait<false>(q_own_free, 0, abort_flag, p.status);
       }
       for (int it = 0; ok && it < ntiles; ++it) {
         const int so = it % kOwnStages, ro = it / kOwnStages;
