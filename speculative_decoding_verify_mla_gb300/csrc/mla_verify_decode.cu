@@ -266,9 +266,10 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       mbar_init(p_full(b), 128);
       mbar_init(pv_done(b), 1);
     }
-    // 128 softmax threads (TMEM half) + the other half: the producer's TMA
-    // (bf16) or the 128 converter threads (fp8 KV, f16 query)
-    mbar_init(q_ready, kF8 ? 128 + 128 : 128 + 1);
+    // 128 softmax threads (the TMEM half), + the 128 converter threads with
+    // fp8 KV (the other half, converted to f16); the bf16 other half is
+    // waited for on q_tma
+    mbar_init(q_ready, kF8 ? 128 + 128 : 128);
     mbar_init(drain_bar, 1);
     mbar_init(gate_full, 1);
     mbar_init(q_tma, 1);
@@ -276,6 +277,18 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
     mbar_init(q_own_free, 128);
     *abort_flag = 0;
     fence_mbar_init_cluster();
+    // both latent halves of the unit's 128 query rows, at once (they depend
+    // on the unit only): this CTA's half staged in the idle other-half ring
+    // for the softmax warps to move into TMEM, the other half into its own
+    // region (A of the SMEM score GEMM; fp8 KV: converted to f16 in place)
+    mbar_arrive_expect_tx(q_own_full, kQHalfBytes);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      tma_load_3d(oth0 + b * kQBoxBytes, &tmap_q, q_own_full, half * kDHalf + b * 64, m_tile * kMTile, r);
+    mbar_arrive_expect_tx(q_tma, kQHalfBytes);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_tma, (1 - half) * kDHalf + b * 64, m_tile * kMTile, r);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -308,21 +321,6 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ntiles > 0) {
-      // this CTA's latent half of the unit's 128 query rows, staged in the
-      // idle other-half ring for the softmax warps to move into TMEM (one
-      // bulk copy instead of 64 KB of per-thread loads)
-      mbar_arrive_expect_tx(q_own_full, kQHalfBytes);
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-        tma_load_3d(oth0 + b * kQBoxBytes, &tmap_q, q_own_full, half * kDHalf + b * 64, m_tile * kMTile, r);
-      // the other latent half of this unit's 128 query rows (A of the SMEM
-      // score GEMM); fp8 KV: bf16, converted to f16 in place by the converters
-      const uint32_t q_bar = kF8 ? q_tma : q_ready;
-      mbar_arrive_expect_tx(q_bar, kQHalfBytes);
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-        tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_bar, (1 - half) * kDHalf + b * 64,
-                    m_tile * kMTile, r);
       if constexpr (!kF8) {
       tma_prefetch_desc(&tmap_kv);
       int last_own[kOwnStages];
@@ -361,7 +359,7 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       }
       // every copy this CTA started has landed before teardown
       drain_wait(q_own_full, 0);
-      drain_wait(q_ready, 0);
+      drain_wait(q_tma, 0);
       for (int s = 0; s < kOwnStages; ++s)
         if (last_own[s] >= 0) drain_wait(own_full(s), last_own[s] & 1);
       for (int s = 0; s < kOthStages; ++s)
@@ -372,6 +370,10 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
         drain_wait(q_own_full, 0);
         drain_wait(q_tma, 0);
       }
+    } else if (lane == 0) {
+      // an empty unit: only the query copies were started
+      drain_wait(q_own_full, 0);
+      drain_wait(q_tma, 0);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -379,7 +381,8 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
     constexpr uint32_t idesc_s = kF8 ? idesc_f16_f32(128, 64, false, false) : idesc_bf16_f32(128, 64, false, false);
     constexpr uint32_t idesc_pv = kF8 ? idesc_f16_f32(128, 256, false, true) : idesc_bf16_f32(128, 256, false, true);
     const uint64_t q_desc = sdesc_sw128(q_s, 16, 1024);  // A of the other-half score MMAs
-    bool ok = ntiles > 0 && warp_wait(q_ready, 0, abort_flag, p.status);
+    bool ok = ntiles > 0 && warp_wait(q_ready, 0, abort_flag, p.status) &&
+              (kF8 || warp_wait(q_tma, 0, abort_flag, p.status));
     bool issued = false;
     auto issue_pv = [&](int i) -> bool {
       const int sb = i & 1;
@@ -518,7 +521,11 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
         tma_load_3d(q_s + b * kQBoxBytes, &tmap_gate, gate_full, half * kDHalf + b * 64,
                     m_tile * kMTile, r);
     };
-    if (fused_gate && p.gate_dim != 1 && ntiles == 0 && leader) load_gate();
+    // an empty unit stages the gate at once, after the query copy into the
+    // same region has landed
+    if (fused_gate && p.gate_dim != 1 && ntiles == 0 && leader &&
+        mbar_wait<false>(q_tma, 0, abort_flag, p.status))
+      load_gate();
 
     float m_ref = -INFINITY;  // running max (log2 units) used for exponentiation
     float l_sum = 0.f;
