@@ -46,11 +46,13 @@
 //  * Work units.  Uniform splits decode the unit from blockIdx; the balanced
 //    plan (a one-CTA plan kernel, this grid its programmatic dependent) hands
 //    each CTA a unit of a list ordered longest first.
-//  * MMA issue.  One thread issues every MMA, so each ring slot's descriptor
-//    is built once and a K step adds a constant to its low word.
-//  * Roles: warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 softmax and
-//    epilogue; the fp8-KV instance adds converter warps 6-9.  Every wait is
-//    bounded; nothing traps.
+//  * MMA issue.  Two issuing threads (scores; P V), so the tensor pipe is fed
+//    from two warps; each ring slot's descriptor is built once and a K step
+//    adds a constant to its low word.
+//  * Roles: warp 0 TMA producer, warp 1 score-MMA issuer, warps 2-5 softmax
+//    and epilogue, one more warp the P V issuer (warp 6; warp 10 in the
+//    fp8-KV instance, whose warps 6-9 convert).  Every wait is bounded;
+//    nothing traps.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -100,8 +102,9 @@ struct KernelShape {
   static constexpr int kOwnStages = 3;
   static constexpr int kOthStages = 2;
   static constexpr int kF8Stages = 0;
-  static constexpr int kThreads = kF8 ? 320 : 192;
-  static constexpr int kNumBars = 22;
+  static constexpr int kThreads = kF8 ? 352 : 224;
+  static constexpr int kPvWarp = kF8 ? 10 : 6;  // issues the P V MMAs
+  static constexpr int kNumBars = 23;
   static constexpr int kFullCount = kF8 ? 128 : 1;  // arrivals completing a KV ring slot
   // shared memory map (offsets from the 1024-aligned base)
   static constexpr int kOffQ = 0;
@@ -203,6 +206,7 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
   auto pv_done = [&](int b) { return bar0 + 8u * (14 + b); };
   const uint32_t q_ready = bar0 + 8u * 16;  // Q own half in TMEM + Q other half in SMEM
   const uint32_t drain_bar = bar0 + 8u * 17;
+  const uint32_t drain_pv = bar0 + 8u * 22;  // the P V issuer's MMAs have completed
   const uint32_t gate_full = bar0 + 8u * 18;  // gate tile staged in the Q region
   const uint32_t q_tma = bar0 + 8u * 19;      // fp8 KV: bf16 query half landed (converted in place)
   // this CTA's query half, TMA-staged in the idle other-half ring, landed /
@@ -271,6 +275,7 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
     // waited for on q_tma
     mbar_init(q_ready, kF8 ? 128 + 128 : 128);
     mbar_init(drain_bar, 1);
+    mbar_init(drain_pv, 1);
     mbar_init(gate_full, 1);
     mbar_init(q_tma, 1);
     mbar_init(q_own_full, 1);
@@ -379,35 +384,10 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_s = kF8 ? idesc_f16_f32(128, 64, false, false) : idesc_bf16_f32(128, 64, false, false);
-    constexpr uint32_t idesc_pv = kF8 ? idesc_f16_f32(128, 256, false, true) : idesc_bf16_f32(128, 256, false, true);
     const uint64_t q_desc = sdesc_sw128(q_s, 16, 1024);  // A of the other-half score MMAs
     bool ok = ntiles > 0 && warp_wait(q_ready, 0, abort_flag, p.status) &&
               (kF8 || warp_wait(q_tma, 0, abort_flag, p.status));
     bool issued = false;
-    auto issue_pv = [&](int i) -> bool {
-      const int sb = i & 1;
-      const int so = i % kOwnStages;
-      if (!warp_wait(p_full(sb), (i >> 1) & 1, abort_flag, p.status)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t a = tmem + kTmemS + 64u * sb;
-        // descriptors differ only in the 14-bit start-address field, which
-        // never carries (shared addresses < 256 KB): one add per MMA
-        const uint64_t pv_desc0 = sdesc_sw128(own0 + so * kHalfTileBytes, kBoxBytes, 1024);
-        const uint32_t pv_lo = (uint32_t)pv_desc0, pv_hi = (uint32_t)(pv_desc0 >> 32);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // B = V tile (own half), MN-major: N = 256 latent columns in four
-          // 64-wide boxes (LBO = box stride), K = 16 KV rows per step (SBO = 8-row stride).
-          mma_ts_w(tmem + kTmemO, a + 8u * kk, pv_lo + (uint32_t)((kk * 16 * 128) >> 4), pv_hi, idesc_pv,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(own_empty(so));
-        mma_commit(pv_done(sb));
-      }
-      __syncwarp();
-      return true;
-    };
     auto zero_tail = [&](uint8_t* tile, int rows_valid) {
       // rows no query row of this unit may see: zero them (pool slack may be NaN)
       const int nrows = kTileN - rows_valid;
@@ -426,6 +406,12 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       const int sb = it & 1;
       if (!warp_wait(own_full(so), (it / kOwnStages) & 1, abort_flag, p.status) ||
           !warp_wait(oth_full(sx), (it / kOthStages) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      // the score buffer is free once the P V of two tiles ago (which read
+      // its P) has completed
+      if (it >= 2 && !warp_wait(pv_done(sb), ((it - 2) >> 1) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
@@ -461,15 +447,46 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       }
       __syncwarp();
       issued = true;
-      if (it >= 1 && !issue_pv(it - 1)) {
-        ok = false;
-        break;
-      }
     }
-    if (ok && ntiles > 0) ok = issue_pv(ntiles - 1);
     if (issued && lane == 0) {
       mma_commit(drain_bar);
       drain_wait(drain_bar, 0);
+    }
+    __syncwarp();
+  } else if (warp == K::kPvWarp) {
+    // ------------------------------------------------------------ P V issuer
+    // A second issuing warp: the tensor pipe takes MMAs from both, so the
+    // P V products no longer wait in line behind the score MMAs' issue.
+    // It is the only writer of O (accumulation order unchanged).
+    constexpr uint32_t idesc_pv = kF8 ? idesc_f16_f32(128, 256, false, true) : idesc_bf16_f32(128, 256, false, true);
+    bool issued = false;
+    for (int i = 0; i < ntiles; ++i) {
+      const int sb = i & 1;
+      const int so = i % kOwnStages;
+      if (!warp_wait(p_full(sb), (i >> 1) & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t a = tmem + kTmemS + 64u * sb;
+        // descriptors differ only in the 14-bit start-address field, which
+        // never carries (shared addresses < 256 KB): one add per MMA
+        const uint64_t pv_desc0 = sdesc_sw128(own0 + so * kHalfTileBytes, kBoxBytes, 1024);
+        const uint32_t pv_lo = (uint32_t)pv_desc0, pv_hi = (uint32_t)(pv_desc0 >> 32);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          // B = V tile (own half), MN-major: N = 256 latent columns in four
+          // 64-wide boxes (LBO = box stride), K = 16 KV rows per step (SBO = 8-row stride).
+          mma_ts_w(tmem + kTmemO, a + 8u * kk, pv_lo + (uint32_t)((kk * 16 * 128) >> 4), pv_hi, idesc_pv,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(own_empty(so));
+        mma_commit(pv_done(sb));
+      }
+      __syncwarp();
+      issued = true;
+    }
+    if (issued && lane == 0) {
+      mma_commit(drain_pv);
+      drain_wait(drain_pv, 0);
     }
     __syncwarp();
   } else if (!kF8 || warp < 6) {
@@ -683,7 +700,7 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
   }
 
   if constexpr (kF8) {
-    if (warp >= 6) {
+    if (warp >= 6 && warp < 10) {
       // ---------------------------------------------------------- fp8 converters
       // 128 threads.  First the other latent half of the unit's query rows
       // (TMA-loaded as bf16) is converted to f16 in shared memory.  Then the
