@@ -49,10 +49,10 @@
 //  * MMA issue.  Two issuing threads (scores; P V), so the tensor pipe is fed
 //    from two warps; each ring slot's descriptor is built once and a K step
 //    adds a constant to its low word.
-//  * Roles: warp 0 TMA producer, warp 1 score-MMA issuer, warps 2-5 softmax
-//    and epilogue, one more warp the P V issuer (warp 6; warp 10 in the
-//    fp8-KV instance, whose warps 6-9 convert).  Every wait is bounded;
-//    nothing traps.
+//  * Roles: warp 0 TMA producer, warps 2-5 softmax and epilogue, three MMA
+//    issuers: warp 1 the even tiles' scores, warp 7 the odd tiles' scores,
+//    warp 6 P V (fp8-KV instance: warps 11, 10; its warps 6-9 convert).
+//    Every wait is bounded; nothing traps.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -88,6 +88,7 @@ constexpr float kRescaleThreshold = 8.0f;  // in log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
 constexpr int kF8TileBytes = 64 * kD;  // one fp8 KV tile: 64 rows x 512 e4m3 codes
+constexpr int kTwoIssuerTiles = 8;     // units with this many KV tiles use both score issuers
 
 // Two variants of the kernel.  bf16 KV: the TMA producer fills the bf16 KV
 // rings and every MMA takes bf16 operands.  fp8 KV: the MMAs take f16
@@ -97,14 +98,16 @@ constexpr int kF8TileBytes = 64 * kD;  // one fp8 KV tile: 64 rows x 512 e4m3 co
 // into the same swizzled ring slots, and also write the other query half as
 // f16 into shared memory; the softmax warps put their query half into TMEM
 // as f16 and write P as f16.
-template <bool kF8>
+template <bool kF8, bool kTwo>
 struct KernelShape {
   static constexpr int kOwnStages = 3;
   static constexpr int kOthStages = 2;
   static constexpr int kF8Stages = 0;
-  static constexpr int kThreads = kF8 ? 352 : 224;
+  // kTwo: a second score issuer for the odd tiles (long units)
+  static constexpr int kThreads = (kF8 ? 352 : 224) + (kTwo ? 32 : 0);
   static constexpr int kPvWarp = kF8 ? 10 : 6;  // issues the P V MMAs
-  static constexpr int kNumBars = 23;
+  static constexpr int kOddWarp = kTwo ? (kF8 ? 11 : 7) : -1;  // issues the odd tiles' score MMAs
+  static constexpr int kNumBars = 24;
   static constexpr int kFullCount = kF8 ? 128 : 1;  // arrivals completing a KV ring slot
   // shared memory map (offsets from the 1024-aligned base)
   static constexpr int kOffQ = 0;
@@ -115,10 +118,14 @@ struct KernelShape {
   static constexpr int kSmemUsed = kOffBar + kNumBars * 8 + 16;
   static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
 };
-static_assert(KernelShape<false>::kSmemBytes <= 232448 && KernelShape<true>::kSmemBytes <= 232448,
+static_assert(KernelShape<false, false>::kSmemBytes == KernelShape<false, true>::kSmemBytes &&
+                  KernelShape<false, false>::kSmemBytes == KernelShape<true, false>::kSmemBytes &&
+                  KernelShape<false, false>::kSmemBytes == KernelShape<true, true>::kSmemBytes,
+              "every instance has the same shared-memory map");
+static_assert(KernelShape<false, false>::kSmemBytes <= 232448 && KernelShape<true, true>::kSmemBytes <= 232448,
               "shared memory budget");
-static_assert(KernelShape<false>::kOffBar - KernelShape<false>::kOffOwn >= 4 * kQBoxBytes &&
-                  KernelShape<true>::kOffBar - KernelShape<true>::kOffOwn >= 4 * kQBoxBytes,
+static_assert(KernelShape<false, false>::kOffBar - KernelShape<false, false>::kOffOwn >= 4 * kQBoxBytes &&
+                  KernelShape<true, false>::kOffBar - KernelShape<true, false>::kOffOwn >= 4 * kQBoxBytes,
               "the epilogue stages a 128 x 256 bf16 tile over the idle KV buffers");
 
 struct VerifyParams {
@@ -179,14 +186,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // Tensor maps: tmap_kv 2-D over the page pool [pages*64][512] bf16; tmap_q,
 // tmap_gate, tmap_out 3-D [R][M][512] bf16 (rows past a request's M fall out
 // of bounds: zero on load, dropped on store); tmap_part 4-D [S][R][M][512] fp32.
-template <bool kF8>
-__global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
+template <bool kF8, bool kTwo>
+__global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     mla_verify_kernel(const __grid_constant__ CUtensorMap tmap_kv,
                       const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_gate,
                       const __grid_constant__ CUtensorMap tmap_out,
                       const __grid_constant__ CUtensorMap tmap_part, const VerifyParams p) {
-  using K = KernelShape<kF8>;
+  using K = KernelShape<kF8, kTwo>;
   constexpr int kOwnStages = K::kOwnStages, kOthStages = K::kOthStages, kNumBars = K::kNumBars;
   constexpr int kOffQ = K::kOffQ, kOffOwn = K::kOffOwn, kOffOth = K::kOffOth, kOffBar = K::kOffBar;
   extern __shared__ uint8_t smem_raw[];
@@ -207,6 +214,7 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
   const uint32_t q_ready = bar0 + 8u * 16;  // Q own half in TMEM + Q other half in SMEM
   const uint32_t drain_bar = bar0 + 8u * 17;
   const uint32_t drain_pv = bar0 + 8u * 22;  // the P V issuer's MMAs have completed
+  const uint32_t drain_odd = bar0 + 8u * 23;  // the odd-tile score issuer's MMAs have completed
   const uint32_t gate_full = bar0 + 8u * 18;  // gate tile staged in the Q region
   const uint32_t q_tma = bar0 + 8u * 19;      // fp8 KV: bf16 query half landed (converted in place)
   // this CTA's query half, TMA-staged in the idle other-half ring, landed /
@@ -276,6 +284,7 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
     mbar_init(q_ready, kF8 ? 128 + 128 : 128);
     mbar_init(drain_bar, 1);
     mbar_init(drain_pv, 1);
+    mbar_init(drain_odd, 1);
     mbar_init(gate_full, 1);
     mbar_init(q_tma, 1);
     mbar_init(q_own_full, 1);
@@ -381,11 +390,20 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       drain_wait(q_tma, 0);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || (kTwo && warp == K::kOddWarp)) {
+    // ------------------------------------------------------------ score MMA issuers
+    // Two warps: warp 1 the even tiles (score buffer 0), the other warp the
+    // odd tiles (buffer 1).  Each buffer is written by one warp only, and the
+    // tensor pipe takes MMAs from both (one issuing thread alone issues a
+    // 128 x 64 x 16 MMA no faster than ~45 cycles; the datapath needs 32).
+    // Short units keep one issuer (interleaving tiles 0 and 1 would delay the
+    // first scores, which a short unit waits for).
+    const bool two = kTwo && ntiles >= kTwoIssuerTiles;
+    const int first = (warp == 1) ? 0 : 1;
+    const int step = two ? 2 : 1;
     constexpr uint32_t idesc_s = kF8 ? idesc_f16_f32(128, 64, false, false) : idesc_bf16_f32(128, 64, false, false);
     const uint64_t q_desc = sdesc_sw128(q_s, 16, 1024);  // A of the other-half score MMAs
-    bool ok = ntiles > 0 && warp_wait(q_ready, 0, abort_flag, p.status) &&
+    bool ok = ntiles > 0 && (warp == 1 || two) && warp_wait(q_ready, 0, abort_flag, p.status) &&
               (kF8 || warp_wait(q_tma, 0, abort_flag, p.status));
     bool issued = false;
     auto zero_tail = [&](uint8_t* tile, int rows_valid) {
@@ -400,7 +418,7 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       }
     };
     if (ok) tc_fence_after();
-    for (int it = 0; ok && it < ntiles; ++it) {
+    for (int it = first; ok && it < ntiles; it += step) {
       const int so = it % kOwnStages;
       const int sx = it % kOthStages;
       const int sb = it & 1;
@@ -449,8 +467,9 @@ __global__ void __launch_bounds__(KernelShape<kF8>::kThreads, 1)
       issued = true;
     }
     if (issued && lane == 0) {
-      mma_commit(drain_bar);
-      drain_wait(drain_bar, 0);
+      const uint32_t drain = first == 0 ? drain_bar : drain_odd;
+      mma_commit(drain);
+      drain_wait(drain, 0);
     }
     __syncwarp();
   } else if (warp == K::kPvWarp) {
@@ -967,10 +986,14 @@ bool device_setup(int* sm_count) {
   if (!g_attr_set[dev]) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-    if (cudaFuncSetAttribute(mla_verify_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KernelShape<false>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_verify_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KernelShape<true>::kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(mla_verify_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KernelShape<false, false>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_verify_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KernelShape<false, true>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_verify_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KernelShape<true, false>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_verify_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KernelShape<true, true>::kSmemBytes) != cudaSuccess)
       return false;
     g_sm_count[dev] = sms;
     g_attr_set[dev] = true;
@@ -1180,9 +1203,14 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   // fp8: the pool scale multiplies every score (folded into the scale here)
   // and the output (applied in the epilogue)
   if (kv_fp8) prm.scale_log2 *= kv_scale;
-  auto kernel = kv_fp8 ? mla_verify_kernel<true> : mla_verify_kernel<false>;
-  const int threads = kv_fp8 ? KernelShape<true>::kThreads : KernelShape<false>::kThreads;
-  const int smem = kv_fp8 ? KernelShape<true>::kSmemBytes : KernelShape<false>::kSmemBytes;
+  // long units (uniform splits of >= kTwoIssuerTiles tiles, or the balanced
+  // plan's pieces) take the instance with a second score issuer
+  const bool two = balanced || ((long long)max_pages_per_req + S - 1) / S >= kTwoIssuerTiles;
+  auto kernel = kv_fp8 ? (two ? mla_verify_kernel<true, true> : mla_verify_kernel<true, false>)
+                       : (two ? mla_verify_kernel<false, true> : mla_verify_kernel<false, false>);
+  const int threads = kv_fp8 ? (two ? KernelShape<true, true>::kThreads : KernelShape<true, false>::kThreads)
+                             : (two ? KernelShape<false, true>::kThreads : KernelShape<false, false>::kThreads);
+  const int smem = KernelShape<false, false>::kSmemBytes;  // the same for every instance
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   if (!balanced) {
