@@ -89,7 +89,10 @@ const char* sv_status_string(sv_status s);
  *     o    = sum_j exp(s_j - lse) * c_j                  (0    when b == 0)
  *     out  = sigmoid(gate[t][h]) * o   (elementwise over the 512 columns)
  * The k+1 tokens of a request are folded into M = H*(k+1) query rows that
- * share the request's KV (row = t_local*H + h), processed as 128-row tiles.
+ * share the request's KV (row = t_local*H + h), processed as 128-row tiles;
+ * each (row tile, KV split) runs on two CTAs, one per 256-column latent half
+ * of the output.  With uniform splits and M <= 64, one CTA may hold both
+ * halves instead (the "stacked" form, see sv_mla_verify_set_stacked).
  *
  * Arguments (all device pointers unless stated):
  *   q_latent      bf16 [T][H][512], 16-byte aligned, contiguous.
@@ -144,6 +147,27 @@ const char* sv_status_string(sv_status s);
  * accepts except 0 (resolve it first). */
 int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pages_per_req);
 size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits);
+
+/* The stacked form of the attention kernels, process-wide for every later
+ * call; returns the previous mode, or -1 (nothing changed) for another value.
+ * The stacked form runs requests of M = H*q_per_req <= 64 query rows with
+ * uniform splits on one CTA per (request, split): rows 64..127 of the CTA's
+ * 128-row MMA tile repeat rows 0..63, and the softmax weights P form a
+ * block-diagonal operand over the KV tile taken twice, so TMEM lanes 0..63
+ * accumulate latent columns 0..255 and lanes 64..127 columns 256..511 (no
+ * second CTA recomputing the scores).  The result is the same beyond
+ * rounding.
+ *   SV_STACKED_OFF     never (two CTAs per unit, one per latent half);
+ *   SV_STACKED_AUTO    (default) when a unit holds at least 4 KV tiles
+ *                      (ceil(max_pages_per_req / S) >= 4);
+ *   SV_STACKED_ALWAYS  whenever M <= 64.
+ * The automatic split count (num_splits = 0) counts one CTA per unit for
+ * the stacked form.  Meant for tests and tuning; not synchronised with
+ * calls in flight on other threads. */
+#define SV_STACKED_OFF 0
+#define SV_STACKED_AUTO 1
+#define SV_STACKED_ALWAYS 2
+int sv_mla_verify_set_stacked(int mode);
 
 sv_status mla_verify_decode(const void* q_latent, const void* kv_pages, int num_pages,
                             int page_size, const int32_t* block_table, int R, int q_per_req,

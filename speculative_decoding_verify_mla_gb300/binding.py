@@ -25,6 +25,7 @@ SV_LATENT_DIM = 512
 SV_PAGE_SIZE = 64
 SV_MAX_SPLITS = 64
 SV_SPLITS_BALANCED = -1
+STACKED_OFF, STACKED_AUTO, STACKED_ALWAYS = 0, 1, 2
 SV_DEV_BAD_PAGE = 0x1
 SV_DEV_BAD_BOUND = 0x2
 SV_DEV_TIMEOUT = 0x4
@@ -43,6 +44,7 @@ EXPORTED_SYMBOLS = (
     "mla_verify_decode_gated",
     "mla_wuv_project",
     "mla_verify_decode_kv8",
+    "sv_mla_verify_set_stacked",
 )
 
 _lib = None
@@ -71,6 +73,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.sv_status_string.restype = ctypes.c_char_p
         lib.sv_mla_verify_num_splits.argtypes = [_c_int, _c_int, _c_int, _c_int]
         lib.sv_mla_verify_num_splits.restype = _c_int
+        lib.sv_mla_verify_set_stacked.argtypes = [_c_int]
+        lib.sv_mla_verify_set_stacked.restype = _c_int
         lib.sv_mla_verify_workspace_bytes.argtypes = [_c_int, _c_int, _c_int]
         lib.sv_mla_verify_workspace_bytes.restype = _c_size
         lib.mla_verify_decode.argtypes = [
@@ -137,6 +141,16 @@ def _check_status(func: str, code: int):
 
 def num_splits_for(R: int, q_per_req: int, H: int, max_pages_per_req: int) -> int:
     return int(load_library().sv_mla_verify_num_splits(R, q_per_req, H, max_pages_per_req))
+
+
+def set_stacked(mode: int) -> int:
+    """Mode of the stacked attention form (one CTA per unit for requests of
+    <= 64 query rows) for the process: STACKED_OFF, STACKED_AUTO (default)
+    or STACKED_ALWAYS; returns the previous mode."""
+    prev = int(load_library().sv_mla_verify_set_stacked(int(mode)))
+    if prev < 0:
+        raise ValueError(f"unknown stacked mode {mode}")
+    return prev
 
 
 def attention_workspace_bytes(T: int, H: int, num_splits: int) -> int:

@@ -49,6 +49,14 @@
 //  * MMA issue.  Two issuing threads (scores; P V), so the tensor pipe is fed
 //    from two warps; each ring slot's descriptor is built once and a K step
 //    adds a constant to its low word.
+//  * Stacked instance (M <= 64 query rows, uniform splits).  One
+//    CTA holds both latent halves: rows 64..127 of its 128-row tile repeat
+//    rows 0..63 (the other query half is TMA-loaded twice), so score rows L
+//    and L + 64 are equal; the softmax writes P block-diagonally ([P | 0] in
+//    lanes 0..63, [0 | P] in lanes 64..127) and P V runs K = 128 over the
+//    tile's two latent halves, so lanes 0..63 of O accumulate latent
+//    0..255 and lanes 64..127 latent 256..511.  No second CTA recomputes
+//    the scores; the other-half ring is released after P V.
 //  * Roles: warp 0 TMA producer, warps 2-5 softmax and epilogue, three MMA
 //    issuers: warp 1 the even tiles' scores, warp 7 the odd tiles' scores,
 //    warp 6 P V (fp8-KV instance: warps 11, 10; its warps 6-9 convert).
@@ -58,6 +66,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -186,7 +195,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // Tensor maps: tmap_kv 2-D over the page pool [pages*64][512] bf16; tmap_q,
 // tmap_gate, tmap_out 3-D [R][M][512] bf16 (rows past a request's M fall out
 // of bounds: zero on load, dropped on store); tmap_part 4-D [S][R][M][512] fp32.
-template <bool kF8, bool kTwo>
+template <bool kF8, bool kTwo, bool kStack>
 __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     mla_verify_kernel(const __grid_constant__ CUtensorMap tmap_kv,
                       const __grid_constant__ CUtensorMap tmap_q,
@@ -243,8 +252,9 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     slot = u.w;
     fused = slot < 0;
   } else {
-    half = blockIdx.x & 1;  // latent half of O owned by this CTA
-    const int unit = blockIdx.x >> 1;
+    // latent half of O owned by this CTA (stacked: both, in the two lane halves)
+    half = kStack ? 0 : (int)(blockIdx.x & 1);
+    const int unit = kStack ? (int)blockIdx.x : (int)(blockIdx.x >> 1);
     s_idx = unit % S;
     const int rm = unit / S;
     m_tile = rm % p.n_mtiles;
@@ -295,14 +305,30 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     // on the unit only): this CTA's half staged in the idle other-half ring
     // for the softmax warps to move into TMEM, the other half into its own
     // region (A of the SMEM score GEMM; fp8 KV: converted to f16 in place)
-    mbar_arrive_expect_tx(q_own_full, kQHalfBytes);
+    if constexpr (!kStack) {
+      mbar_arrive_expect_tx(q_own_full, kQHalfBytes);
 #pragma unroll
-    for (int b = 0; b < 4; ++b)
-      tma_load_3d(oth0 + b * kQBoxBytes, &tmap_q, q_own_full, half * kDHalf + b * 64, m_tile * kMTile, r);
-    mbar_arrive_expect_tx(q_tma, kQHalfBytes);
+      for (int b = 0; b < 4; ++b)
+        tma_load_3d(oth0 + b * kQBoxBytes, &tmap_q, q_own_full, half * kDHalf + b * 64, m_tile * kMTile, r);
+      mbar_arrive_expect_tx(q_tma, kQHalfBytes);
 #pragma unroll
-    for (int b = 0; b < 4; ++b)
-      tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_tma, (1 - half) * kDHalf + b * 64, m_tile * kMTile, r);
+      for (int b = 0; b < 4; ++b)
+        tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_tma, (1 - half) * kDHalf + b * 64, m_tile * kMTile, r);
+    } else {
+      // stacked: tmap_q has 64-row boxes.  Latent 0..255 of the (at most 64)
+      // query rows into rows 0..63 of the staging boxes; latent 256..511
+      // twice, into rows 0..63 and 64..127 of the SMEM A operand, so that
+      // score rows L and L + 64 are the same query row.
+      mbar_arrive_expect_tx(q_own_full, kQHalfBytes / 2);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) tma_load_3d(oth0 + b * kQBoxBytes, &tmap_q, q_own_full, b * 64, 0, r);
+      mbar_arrive_expect_tx(q_tma, kQHalfBytes);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_tma, kDHalf + b * 64, 0, r);
+        tma_load_3d(q_s + b * kQBoxBytes + kQBoxBytes / 2, &tmap_q, q_tma, kDHalf + b * 64, 0, r);
+      }
+    }
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -461,7 +487,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
                    kx_lo + (uint32_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4), k_hi, idesc_s, 1u);
         }
         mma_commit(s_full(sb));
-        mma_commit(oth_empty(sx));
+        if constexpr (!kStack) mma_commit(oth_empty(sx));  // stacked: P V reads it too
       }
       __syncwarp();
       issued = true;
@@ -482,6 +508,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     for (int i = 0; i < ntiles; ++i) {
       const int sb = i & 1;
       const int so = i % kOwnStages;
+      const int sx = i % kOthStages;
       if (!warp_wait(p_full(sb), (i >> 1) & 1, abort_flag, p.status)) break;
       tc_fence_after();
       if (lane == 0) {
@@ -490,12 +517,25 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         // never carries (shared addresses < 256 KB): one add per MMA
         const uint64_t pv_desc0 = sdesc_sw128(own0 + so * kHalfTileBytes, kBoxBytes, 1024);
         const uint32_t pv_lo = (uint32_t)pv_desc0, pv_hi = (uint32_t)(pv_desc0 >> 32);
+        if constexpr (kStack) {
+          // P is block-diagonal over K = 128: lanes 64..127 hold [0 | P] and
+          // accumulate latent 256..511 from the other ring's tile; lanes
+          // 0..63 hold [P | 0] and accumulate latent 0..255 from the own
+          // ring's tile below.  The other-ring steps go first so that their
+          // slot (the shallower ring) is released as early as possible.
+          const uint32_t px_lo = (uint32_t)sdesc_sw128(oth0 + sx * kHalfTileBytes, kBoxBytes, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts_w(tmem + kTmemO, a + 32u + 8u * kk, px_lo + (uint32_t)((kk * 16 * 128) >> 4), pv_hi, idesc_pv,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(oth_empty(sx));
+        }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           // B = V tile (own half), MN-major: N = 256 latent columns in four
           // 64-wide boxes (LBO = box stride), K = 16 KV rows per step (SBO = 8-row stride).
           mma_ts_w(tmem + kTmemO, a + 8u * kk, pv_lo + (uint32_t)((kk * 16 * 128) >> 4), pv_hi, idesc_pv,
-                   (i > 0 || kk > 0) ? 1u : 0u);
+                   (kStack || i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(own_empty(so));
         mma_commit(pv_done(sb));
@@ -514,7 +554,9 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     const int i = wq * 32 + lane;
     const bool leader = (warp == 2 && lane == 0);
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const int f = m_tile * kMTile + i;
+    // stacked: lane i holds query row i mod 64 and latent half i / 64 of O
+    const int qi = kStack ? (i & 63) : i;
+    const int f = m_tile * kMTile + qi;
     const bool valid = f < Mq;
     const int t_loc = valid ? f / p.H : 0;
     const long long row_g = (long long)r * Mq + f;
@@ -525,7 +567,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       // this CTA's half of the query row, staged by TMA (row i of box c at
       // c * 16 KB + 128 i, 16-byte chunks swizzled by i mod 8) -> TMEM (bf16
       // pairs per 32-bit column); rows past M arrived as zeros
-      const uint8_t* const qrow = sptr + kOffOth + i * 128;
+      const uint8_t* const qrow = sptr + kOffOth + qi * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
@@ -552,10 +594,19 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     // score GEMM will read it again.
     auto load_gate = [&]() {
       mbar_arrive_expect_tx(gate_full, kQHalfBytes);
+      if constexpr (!kStack) {
 #pragma unroll
-      for (int b = 0; b < 4; ++b)
-        tma_load_3d(q_s + b * kQBoxBytes, &tmap_gate, gate_full, half * kDHalf + b * 64,
-                    m_tile * kMTile, r);
+        for (int b = 0; b < 4; ++b)
+          tma_load_3d(q_s + b * kQBoxBytes, &tmap_gate, gate_full, half * kDHalf + b * 64,
+                      m_tile * kMTile, r);
+      } else {
+        // rows 64h .. 64h+63 of box b: latent 256h + 64b .. +63 (64-row boxes)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          tma_load_3d(q_s + b * kQBoxBytes, &tmap_gate, gate_full, b * 64, 0, r);
+          tma_load_3d(q_s + b * kQBoxBytes + kQBoxBytes / 2, &tmap_gate, gate_full, kDHalf + b * 64, 0, r);
+        }
+      }
     };
     // an empty unit stages the gate at once, after the query copy into the
     // same region has landed
@@ -629,7 +680,18 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         pk[c] = kF8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
       }
       l_sum += psum;
-      tmem_st32(tmem + lane_off + kTmemS + 64u * sb, pk);  // P over the consumed scores
+      if constexpr (!kStack) {
+        tmem_st32(tmem + lane_off + kTmemS + 64u * sb, pk);  // P over the consumed scores
+      } else {
+        // block-diagonal A of the stacked P V: [P | 0] in lanes 0..63, [0 | P]
+        // in lanes 64..127 (K = 128: this tile's 64 KV rows twice)
+        uint32_t zero[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) zero[c] = 0u;
+        const uint32_t pcol = (i < 64) ? 0u : 32u;
+        tmem_st32(tmem + lane_off + kTmemS + 64u * sb + pcol, pk);
+        tmem_st32(tmem + lane_off + kTmemS + 64u * sb + (32u - pcol), zero);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full(sb));
@@ -697,15 +759,27 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       fence_proxy_async_smem();
       named_bar_sync(kEpilogueBarId, 128);
       if (leader) {
-        if (fused_gate)
-          tma_store_3d(&tmap_out, st0 + bx * kQBoxBytes, half * kDHalf + bx * 64, m_tile * kMTile, r);
-        else
-          tma_store_4d(&tmap_part, st0 + bx * kQBoxBytes, half * kDHalf + bx * 64, m_tile * kMTile,
-                       p.units ? 0 : r, p.units ? slot : s_idx);
+        if constexpr (!kStack) {
+          if (fused_gate)
+            tma_store_3d(&tmap_out, st0 + bx * kQBoxBytes, half * kDHalf + bx * 64, m_tile * kMTile, r);
+          else
+            tma_store_4d(&tmap_part, st0 + bx * kQBoxBytes, half * kDHalf + bx * 64, m_tile * kMTile,
+                         p.units ? 0 : r, p.units ? slot : s_idx);
+        } else {
+          // staged rows 64h .. 64h+63 are latent 256h + 64bx .. +63 (64-row boxes)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t src = st0 + bx * kQBoxBytes + h * (kQBoxBytes / 2);
+            if (fused_gate)
+              tma_store_3d(&tmap_out, src, h * kDHalf + bx * 64, 0, r);
+            else
+              tma_store_4d(&tmap_part, src, h * kDHalf + bx * 64, 0, r, s_idx);
+          }
+        }
         tma_store_commit();
       }
     }
-    if (valid && half == 0) {
+    if (valid && (kStack ? i < 64 : half == 0)) {
       if (fused_gate) {
         p.lse[row_g] = lse_v;
       } else {
@@ -986,14 +1060,16 @@ bool device_setup(int* sm_count) {
   if (!g_attr_set[dev]) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-    if (cudaFuncSetAttribute(mla_verify_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KernelShape<false, false>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_verify_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KernelShape<false, true>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_verify_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KernelShape<true, false>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_verify_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KernelShape<true, true>::kSmemBytes) != cudaSuccess)
+    constexpr int smem = KernelShape<false, false>::kSmemBytes;  // the same for every instance
+    constexpr auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    if (cudaFuncSetAttribute(mla_verify_kernel<false, false, false>, attr, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_verify_kernel<false, true, false>, attr, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_verify_kernel<true, false, false>, attr, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_verify_kernel<true, true, false>, attr, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_verify_kernel<false, false, true>, attr, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_verify_kernel<false, true, true>, attr, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_verify_kernel<true, false, true>, attr, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(mla_verify_kernel<true, true, true>, attr, smem) != cudaSuccess)
       return false;
     g_sm_count[dev] = sms;
     g_attr_set[dev] = true;
@@ -1002,19 +1078,43 @@ bool device_setup(int* sm_count) {
   return true;
 }
 
+// The stacked instance (both latent halves in one CTA, stacked in the TMEM
+// lanes) serves requests of at most 64 query rows.  Its KV rings are two
+// tiles deep (a tile holds both ring slots until its P V completes), so it
+// pays only when a unit holds several tiles: measured on the C = 64 plain
+// decode batch (20 tiles per request) 47.5 us against 51.0 us for the
+// two-CTA form, and slower than it on 1-2 tile units.  Process-wide mode,
+// see sv_mla_verify_set_stacked.
+constexpr int kStackMinTiles = 4;
+std::atomic<int> g_stack_mode{SV_STACKED_AUTO};
+inline int stack_mode() { return g_stack_mode.load(std::memory_order_relaxed); }
+// Stacked form for units of ceil(max_pages / S) tiles?
+inline bool use_stack(long long Mq, long long max_pages, long long S) {
+  const int m = stack_mode();
+  if (Mq > 64 || m == SV_STACKED_OFF) return false;
+  return m == SV_STACKED_ALWAYS || (max_pages + S - 1) / S >= kStackMinTiles;
+}
+
 // Splits: enough (request, row tile, split, latent half) CTAs to fill the SMs
 // once, each split keeping at least 2 KV tiles (on the C = 1 verify batch,
-// 24 tiles: 12 splits 22.7 us, 8: 22.9, 6: 24.7, 19: 24.9 measured).
-int auto_splits(int R, int q_per_req, int H, int max_pages, int sm_count) {
-  const long long n_mt = ((long long)H * q_per_req + kMTile - 1) / kMTile;
-  const long long ctas = 2ll * R * n_mt;
-  if (ctas <= 0) return 1;
-  long long s = (long long)sm_count / ctas;
+// 24 tiles: 12 splits 22.7 us, 8: 22.9, 6: 24.7, 19: 24.9 measured).  A
+// stacked unit is one CTA per (request, split).
+int fill_splits(long long ctas_per_split, int max_pages, int sm_count) {
+  if (ctas_per_split <= 0) return 1;
+  long long s = (long long)sm_count / ctas_per_split;
   const long long by_len = max_pages / 2;
   if (s > by_len) s = by_len;
   if (s > SV_MAX_SPLITS) s = SV_MAX_SPLITS;
   if (s < 1) s = 1;
   return (int)s;
+}
+int auto_splits(int R, int q_per_req, int H, int max_pages, int sm_count) {
+  const long long Mq = (long long)H * q_per_req;
+  const long long n_mt = (Mq + kMTile - 1) / kMTile;
+  // the stacked form if its own split count leaves it long enough units
+  const int s_stack = fill_splits((long long)R * n_mt, max_pages, sm_count);
+  if (use_stack(Mq, max_pages, s_stack)) return s_stack;
+  return fill_splits(2ll * R * n_mt, max_pages, sm_count);
 }
 
 inline bool misaligned(const void* p, uintptr_t a) {
@@ -1074,6 +1174,11 @@ extern "C" int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pag
   if (R >= 2 && max_pages_per_req >= 64 && max_pages_per_req <= 0xFFFF && 2 * n_mt * R <= sms)
     return SV_SPLITS_BALANCED;
   return sv::auto_splits(R, q_per_req, H, max_pages_per_req, sms);
+}
+
+extern "C" int sv_mla_verify_set_stacked(int mode) {
+  if (mode != SV_STACKED_OFF && mode != SV_STACKED_AUTO && mode != SV_STACKED_ALWAYS) return -1;
+  return sv::g_stack_mode.exchange(mode);
 }
 
 extern "C" size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits) {
@@ -1145,12 +1250,16 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   }
   if (!get_encode_fn()) return SV_ERR_DEVICE;
   const long long Mq = (long long)H * q_per_req;
+  // stacked instance: requests of <= 64 query rows, uniform splits; its row
+  // maps have 64-row boxes
+  const bool stack = !balanced && use_stack(Mq, max_pages_per_req, S);
+  const int m_box = stack ? 64 : kMTile;
   CUtensorMap tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part;
   {
     const cuuint64_t kv_dims[2] = {(cuuint64_t)kD, (cuuint64_t)num_pages * kTileN};
     const cuuint32_t kv_box[2] = {64, (cuuint32_t)kTileN};
     const cuuint64_t row_dims[3] = {(cuuint64_t)kD, (cuuint64_t)Mq, (cuuint64_t)R};
-    const cuuint32_t row_box[3] = {64, (cuuint32_t)kMTile, 1};
+    const cuuint32_t row_box[3] = {64, (cuuint32_t)m_box, 1};
     const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     // fp8 KV is read by the converter warps, not through a tensor map
     if ((kv_fp8 ? !encode_map(&tmap_kv, bf16, 2, q_latent, 3, row_dims, row_box)
@@ -1167,7 +1276,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
         return SV_ERR_ALIGN;
     } else if (S > 1) {
       const cuuint64_t part_dims[4] = {(cuuint64_t)kD, (cuuint64_t)Mq, (cuuint64_t)R, (cuuint64_t)S};
-      const cuuint32_t part_box[4] = {64, (cuuint32_t)kMTile, 1, 1};
+      const cuuint32_t part_box[4] = {64, (cuuint32_t)m_box, 1, 1};
       if (!encode_map(&tmap_part, bf16, 2, part_o, 4, part_dims, part_box))
         return SV_ERR_ALIGN;
     } else {
@@ -1206,15 +1315,17 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   // long units (uniform splits of >= kTwoIssuerTiles tiles, or the balanced
   // plan's pieces) take the instance with a second score issuer
   const bool two = balanced || ((long long)max_pages_per_req + S - 1) / S >= kTwoIssuerTiles;
-  auto kernel = kv_fp8 ? (two ? mla_verify_kernel<true, true> : mla_verify_kernel<true, false>)
-                       : (two ? mla_verify_kernel<false, true> : mla_verify_kernel<false, false>);
+  auto kernel = kv_fp8 ? (stack ? (two ? mla_verify_kernel<true, true, true> : mla_verify_kernel<true, false, true>)
+                               : (two ? mla_verify_kernel<true, true, false> : mla_verify_kernel<true, false, false>))
+                       : (stack ? (two ? mla_verify_kernel<false, true, true> : mla_verify_kernel<false, false, true>)
+                                : (two ? mla_verify_kernel<false, true, false> : mla_verify_kernel<false, false, false>));
   const int threads = kv_fp8 ? (two ? KernelShape<true, true>::kThreads : KernelShape<true, false>::kThreads)
                              : (two ? KernelShape<false, true>::kThreads : KernelShape<false, false>::kThreads);
   const int smem = KernelShape<false, false>::kSmemBytes;  // the same for every instance
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   if (!balanced) {
-    const long long ctas = 2ll * R * prm.n_mtiles * S;
+    const long long ctas = (stack ? 1ll : 2ll) * R * prm.n_mtiles * S;
     if (ctas > 0x7FFFFFFFll) return SV_ERR_SHAPE;
     kernel<<<(unsigned)ctas, threads, smem, st>>>(tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part,
                                                   prm);

@@ -151,6 +151,36 @@ def test_auto_split_choice(lib):
     assert num_splits_for(32, 5, 64, 24) >= 1      # short contexts: uniform splits
 
 
+def test_stacked_switch(lib):
+    """The stacked-form mode is process-wide, returns the previous mode,
+    rejects unknown modes and changes the automatic split count for requests
+    of <= 64 query rows (one CTA per unit instead of two, when the units
+    stay >= 4 tiles long); larger requests are unaffected."""
+    import speculative_decoding_verify_mla_gb300 as sv
+    sms = 152  # no device here: the library's fallback SM count
+    prev = sv.set_stacked(sv.STACKED_AUTO)
+    try:
+        assert sv.set_stacked(sv.STACKED_AUTO) == sv.STACKED_AUTO
+        auto = sv.num_splits_for(64, 1, 64, 24)
+        short = sv.num_splits_for(2, 4, 8, 2)
+        wide_auto = sv.num_splits_for(1, 8, 64, 24)
+        assert sv.set_stacked(sv.STACKED_ALWAYS) == sv.STACKED_AUTO
+        always_short = sv.num_splits_for(2, 4, 8, 8)
+        assert sv.set_stacked(sv.STACKED_OFF) == sv.STACKED_ALWAYS
+        off = sv.num_splits_for(64, 1, 64, 24)
+        off_short = sv.num_splits_for(2, 4, 8, 8)
+        wide_off = sv.num_splits_for(1, 8, 64, 24)
+        with pytest.raises(ValueError):
+            sv.set_stacked(7)
+        assert sv.set_stacked(sv.STACKED_OFF) == sv.STACKED_OFF
+    finally:
+        sv.set_stacked(prev)
+    assert auto == min(sms // 64, 24 // 2) and off == min(sms // 128, 24 // 2)
+    assert short == 1                              # 2-page units: the two-CTA form, 1 split
+    assert always_short == 4 and off_short == 4    # 8 pages: min(SMs / CTAs per split, 8 / 2)
+    assert wide_auto == wide_off
+
+
 def test_gated_and_wuv_host_checks(lib):
     args = dict(q=1 << 12, kv=1 << 12, num_pages=4, page_size=64, bt=1 << 12, R=2, qpr=4, maxp=2,
                 bounds=1 << 12, gate=1 << 12, H=8, scale=0.1, splits=1, ws=None, ws_bytes=0,

@@ -57,6 +57,30 @@ def test_kv8_splits_and_plan(sv, splits):
     check_attention(out, lse, ref_o, ref_l, label=f"kv8 splits={splits}")
 
 
+@pytest.mark.parametrize("mode", ["always", "off"])
+@pytest.mark.parametrize("H,k,lens", [(64, 0, (1100, 64, 4, 700)), (16, 3, (333, 65, 4)), (8, 3, (64, 100))])
+def test_kv8_stacked_form(sv, mode, H, k, lens):
+    """Requests of <= 64 query rows over an fp8 pool, with the stacked form
+    (one CTA holding both latent halves) forced on and off; zero bounds and
+    the head-wise gate included."""
+    cfg = small_config("c0", R=len(lens), k=k, H=H, kv_lens=lens, shuffled=True, vocab=64)
+    inp = make_inputs(cfg, seed=52)
+    bounds = inp["kv_bounds"].copy()
+    bounds[0] = 0
+    g_head = np.ascontiguousarray(inp["gate_bits"][:, :, 0])
+    prev = sv.set_stacked(sv.STACKED_ALWAYS if mode == "always" else sv.STACKED_OFF)
+    try:
+        for splits in (1, 3, 0):
+            status = torch.zeros(1, dtype=torch.int32, device=DEV)
+            out, lse, ref_o, ref_l = _run(sv, inp, splits, bounds=bounds, status=status)
+            assert int(status.item()) == 0
+            check_attention(out, lse, ref_o, ref_l, label=f"kv8 stacked={mode} H={H} k={k} splits={splits}")
+        out, lse, ref_o, ref_l = _run(sv, inp, 2, gate=g_head, bounds=bounds)
+        check_attention(out, lse, ref_o, ref_l, label=f"kv8 stacked={mode} head gate")
+    finally:
+        sv.set_stacked(prev)
+
+
 def test_kv8_zero_bounds_headwise_h96(sv):
     cfg = small_config("c0", R=3, k=1, H=96, kv_lens=(300, 129, 800), shuffled=True, vocab=64)
     inp = make_inputs(cfg, seed=51)

@@ -282,9 +282,15 @@ def test_fold_equals_single_token_decode(sv):
                                     inp["softmax_scale"], num_splits=1)
     k1 = 4
     bt1 = torch.repeat_interleave(d["block_table"], k1, dim=0).contiguous()
-    out1, lse1 = sv.mla_verify_decode(d["q"], d["kv"], bt1, d["kv_bounds"], d["gate"], 1,
-                                      inp["softmax_scale"], num_splits=1)
-    torch.cuda.synchronize()
+    # one-token requests have 64 query rows: keep them on the same (two-CTA)
+    # form as the verify groups
+    prev = sv.set_stacked(sv.STACKED_OFF)
+    try:
+        out1, lse1 = sv.mla_verify_decode(d["q"], d["kv"], bt1, d["kv_bounds"], d["gate"], 1,
+                                          inp["softmax_scale"], num_splits=1)
+        torch.cuda.synchronize()
+    finally:
+        sv.set_stacked(prev)
     assert torch.equal(out, out1)
     assert torch.equal(lse, lse1)
 
