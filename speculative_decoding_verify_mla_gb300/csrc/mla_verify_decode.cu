@@ -42,7 +42,9 @@
 //    query region after the last score MMA), bf16 out + lse.  Several
 //    splits: bf16 o/l and fp32 lse partials for the LSE merge.  The output
 //    leaves in four 64-column boxes by TMA stores, each started as soon as
-//    its box is staged.
+//    its box is staged.  In the long-unit instances four warps (one per TMEM
+//    lane quadrant) are idle by then (fp8: the converters; bf16: producer
+//    and MMA issuers) and take boxes 2..3 of every row.
 //  * Work units.  Uniform splits decode the unit from blockIdx; the balanced
 //    plan (a one-CTA plan kernel, this grid its programmatic dependent) hands
 //    each CTA a unit of a list ordered longest first.
@@ -92,6 +94,8 @@ constexpr int kHalfTileBytes = 4 * kBoxBytes;  // 64 rows x 256 bf16
 constexpr int kQBoxBytes = 128 * 128;          // one Q TMA box: 128 rows x 64 bf16
 constexpr int kQHalfBytes = 4 * kQBoxBytes;    // 128 rows x 256 bf16
 constexpr uint32_t kEpilogueBarId = 1;  // named barrier of the softmax warps
+constexpr uint32_t kHandoffBarId = 2;   // softmax warps + epilogue helper warps
+constexpr uint32_t kHelperBarId = 3;    // named barrier of the epilogue helper warps
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS = 384, kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // in log2 units
 constexpr float kLn2 = 0.6931471805599453f;
@@ -117,6 +121,16 @@ struct KernelShape {
   static constexpr int kPvWarp = kF8 ? 10 : 6;  // issues the P V MMAs
   static constexpr int kOddWarp = kTwo ? (kF8 ? 11 : 7) : -1;  // issues the odd tiles' score MMAs
   static constexpr int kNumBars = 24;
+  // Epilogue helpers of the long-unit instances: four warps, one per TMEM
+  // lane quadrant, whose roles are over by the epilogue (fp8: the
+  // converters; bf16: producer, score issuers and P V issuer).  They stage
+  // and store output boxes 2..3 while the softmax warps do 0..1.  (The
+  // short-unit fp8 instance measured slower with them: c1 23.4 -> 26.0 us.)
+  static constexpr bool kHelp = kTwo;
+  static constexpr int kHelperLeaderWarp = kF8 ? 6 : 0;
+  __host__ __device__ static constexpr bool is_helper(int w) {
+    return kTwo && (kF8 ? (w >= 6 && w < 10) : (w == 0 || w == 1 || w == 6 || w == 7));
+  }
   static constexpr int kFullCount = kF8 ? 128 : 1;  // arrivals completing a KV ring slot
   // shared memory map (offsets from the 1024-aligned base)
   static constexpr int kOffQ = 0;
@@ -124,7 +138,8 @@ struct KernelShape {
   static constexpr int kOffOth = kOffOwn + kOwnStages * kHalfTileBytes;
   static constexpr int kOffF8 = kOffOth + kOthStages * kHalfTileBytes;
   static constexpr int kOffBar = kOffF8 + kF8Stages * kF8TileBytes;
-  static constexpr int kSmemUsed = kOffBar + kNumBars * 8 + 16;
+  static constexpr int kOffRowScale = kOffBar + kNumBars * 8 + 16;  // float[128]: 1/l per TMEM row
+  static constexpr int kSmemUsed = kOffRowScale + 128 * 4;
   static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
 };
 static_assert(KernelShape<false, false>::kSmemBytes == KernelShape<false, true>::kSmemBytes &&
@@ -189,6 +204,108 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_test(bar, parity)) {
     if (globaltimer_ns() - t0 > kWaitTimeoutNs) return;
+  }
+}
+
+// Context of an epilogue box group (see store_boxes).
+struct EpilogueCtx {
+  const VerifyParams* p;
+  const CUtensorMap* tmap_out;
+  const CUtensorMap* tmap_part;
+  uint8_t* sptr;
+  uint32_t sbase, tmem, gate_full;
+  int off_own, off_q;
+  volatile int* abort_flag;
+  int warp, lane, half, m_tile, r, s_idx, slot, Mq;
+  bool fused;
+};
+
+// Epilogue boxes [bx0, bx1) of this thread's TMEM row (row i of lane
+// quadrant warp % 4): O times `scale` (= 1/l; < 0 when the unit produced no
+// O, which stores zeros), gated when this unit finishes its rows (else the
+// split partial), bf16, staged swizzled in the idle KV ring; after each box
+// a named barrier over the 128 threads of the group and `leader` starts its
+// TMA tensor store (rows past M are dropped).  Used by the long-unit
+// instances, whose softmax warps and helper warps split the four boxes.
+template <bool kStack>
+__device__ __forceinline__ void store_boxes(const EpilogueCtx& c, int bx0, int bx1, float scale, uint32_t bar_id,
+                                            bool leader) {
+  const int wq = c.warp & 3;
+  const int i = wq * 32 + c.lane;
+  const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+  const int f = c.m_tile * kMTile + (kStack ? (i & 63) : i);
+  const bool valid = f < c.Mq;
+  const long long row_g = (long long)c.r * c.Mq + f;
+  const bool have_o = scale >= 0.f;
+  const float inv_l = have_o ? scale : 0.f;
+  uint8_t* const stage = c.sptr + c.off_own;
+  const uint32_t row_off = (uint32_t)i * 128u;
+  const uint32_t swz = (uint32_t)(i & 7);
+  // gate: head-wise, one sigmoid per row; elementwise, the staged gate tile;
+  // a partial is not gated (the merge gates)
+  const bool row_gate = c.fused && c.p->gate_dim == 1;
+  const bool elem_gate = c.fused && c.p->gate_dim != 1;
+  float g_row = 1.f;
+  if (row_gate) g_row = valid ? fast_sigmoid(__bfloat162float(c.p->gate[row_g])) : 0.f;
+  const bool gate_ok = elem_gate && warp_wait(c.gate_full, 0, c.abort_flag, c.p->status);
+  const uint8_t* const gs = c.sptr + c.off_q;
+  const uint32_t st0 = c.sbase + c.off_own;
+#pragma unroll 1
+  for (int bx = bx0; bx < bx1; ++bx) {
+    uint32_t va[32], vb[32];  // columns 64 bx .. +31 and 64 bx + 32 .. +63
+    if (have_o) {
+      tmem_ld32(c.tmem + lane_off + kTmemO + 64u * bx, va);
+      tmem_ld32(c.tmem + lane_off + kTmemO + 64u * bx + 32u, vb);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int u = 0; u < 32; ++u) va[u] = vb[u] = 0u;
+    }
+    auto v = [&](int k) { return __uint_as_float(k < 32 ? va[k] : vb[k - 32]); };
+    // 16-byte chunk u of the row holds columns 64 bx + 8u .. +7
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t off = (uint32_t)bx * kQBoxBytes + row_off + (((uint32_t)u ^ swz) << 4);
+      uint32_t ow[4];
+      if (elem_gate) {
+        const uint4 graw = gate_ok ? *reinterpret_cast<const uint4*>(gs + off) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+          ow[e] = pack_bf16x2(v(8 * u + 2 * e) * inv_l * fast_sigmoid(gf.x),
+                              v(8 * u + 2 * e + 1) * inv_l * fast_sigmoid(gf.y));
+        }
+      } else {
+        const float fs = inv_l * g_row;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          ow[e] = pack_bf16x2(v(8 * u + 2 * e) * fs, v(8 * u + 2 * e + 1) * fs);
+      }
+      *reinterpret_cast<uint4*>(stage + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(bar_id, 128);
+    if (leader) {
+      if constexpr (!kStack) {
+        if (c.fused)
+          tma_store_3d(c.tmap_out, st0 + bx * kQBoxBytes, c.half * kDHalf + bx * 64, c.m_tile * kMTile, c.r);
+        else
+          tma_store_4d(c.tmap_part, st0 + bx * kQBoxBytes, c.half * kDHalf + bx * 64, c.m_tile * kMTile,
+                       c.p->units ? 0 : c.r, c.p->units ? c.slot : c.s_idx);
+      } else {
+        // staged rows 64h .. 64h+63 are latent 256h + 64bx .. +63 (64-row boxes)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t src = st0 + bx * kQBoxBytes + h * (kQBoxBytes / 2);
+          if (c.fused)
+            tma_store_3d(c.tmap_out, src, h * kDHalf + bx * 64, 0, c.r);
+          else
+            tma_store_4d(c.tmap_part, src, h * kDHalf + bx * 64, 0, c.r, c.s_idx);
+        }
+      }
+      tma_store_commit();
+    }
   }
 }
 
@@ -561,7 +678,6 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     const int t_loc = valid ? f / p.H : 0;
     const long long row_g = (long long)r * Mq + f;
     const int b_i = valid ? load_bound(p, r * p.q_per_req + t_loc) : 0;
-    const bool fused_gate = fused;
 
     if (ntiles > 0 && warp_wait(q_own_full, 0, abort_flag, p.status)) {
       // this CTA's half of the query row, staged by TMA (row i of box c at
@@ -610,7 +726,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     };
     // an empty unit stages the gate at once, after the query copy into the
     // same region has landed
-    if (fused_gate && p.gate_dim != 1 && ntiles == 0 && leader &&
+    if (fused && p.gate_dim != 1 && ntiles == 0 && leader &&
         mbar_wait<false>(q_tma, 0, abort_flag, p.status))
       load_gate();
 
@@ -621,7 +737,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       const int sb = it & 1;
       const uint32_t par = (it >> 1) & 1;
       if (!warp_wait(s_full(sb), par, abort_flag, p.status)) { ok = false; break; }
-      if (fused_gate && p.gate_dim != 1 && it == ntiles - 1 && leader)
+      if (fused && p.gate_dim != 1 && it == ntiles - 1 && leader)
         load_gate();  // last score GEMM is done
       tc_fence_after();
       float x[64];
@@ -698,9 +814,8 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     }
 
     // ---- epilogue: O/l as bf16 (gated when this unit finishes its rows, else
-    // the split partial), one 64-column box at a time: the box is staged
-    // swizzled in the idle KV ring and the leader starts its TMA tensor store
-    // (rows past M are dropped) while the next box is staged
+    // the split partial), one 64-column box at a time (store_boxes); with
+    // helper warps the softmax warps do boxes 0..1 and hand 1/l over
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // a dependent merge may launch
     if (ok && ntiles > 0)
       ok = warp_wait(pv_done((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
@@ -709,14 +824,25 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     float inv_l = (l_sum > 0.f) ? 1.0f / l_sum : 0.f;
     if constexpr (kF8) inv_l *= p.kv_scale;  // o of the codes -> o of the rows
     const float lse_v = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
+    if constexpr (K::kHelp) {
+      const float scale = have_o ? inv_l : -1.f;
+      // boxes 2..3 of the row go to the helper warp of this lane quadrant
+      reinterpret_cast<float*>(sptr + K::kOffRowScale)[i] = scale;
+      tc_fence_before();
+      named_bar_sync(kHandoffBarId, 256);
+      const EpilogueCtx ctx{&p, &tmap_out, &tmap_part, sptr, sbase, tmem, gate_full, kOffOwn, kOffQ, abort_flag,
+                            warp, lane, half, m_tile, r, s_idx, slot, Mq, fused};
+      store_boxes<kStack>(ctx, 0, 2, scale, kEpilogueBarId, leader);
+    } else {
+    // the same box loop as store_boxes, all four boxes
     // staging: the KV rings are idle once the last P V has completed
     uint8_t* const stage = sptr + kOffOwn;
     const uint32_t row_off = (uint32_t)i * 128u;
     const uint32_t swz = (uint32_t)(i & 7);
     // gate: head-wise, one sigmoid per row; elementwise, the staged gate tile;
     // a partial is not gated (the merge gates)
-    const bool row_gate = fused_gate && p.gate_dim == 1;
-    const bool elem_gate = fused_gate && p.gate_dim != 1;
+    const bool row_gate = fused && p.gate_dim == 1;
+    const bool elem_gate = fused && p.gate_dim != 1;
     float g_row = 1.f;
     if (row_gate) g_row = valid ? fast_sigmoid(__bfloat162float(p.gate[row_g])) : 0.f;
     const bool gate_ok = elem_gate && warp_wait(gate_full, 0, abort_flag, p.status);
@@ -760,7 +886,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       named_bar_sync(kEpilogueBarId, 128);
       if (leader) {
         if constexpr (!kStack) {
-          if (fused_gate)
+          if (fused)
             tma_store_3d(&tmap_out, st0 + bx * kQBoxBytes, half * kDHalf + bx * 64, m_tile * kMTile, r);
           else
             tma_store_4d(&tmap_part, st0 + bx * kQBoxBytes, half * kDHalf + bx * 64, m_tile * kMTile,
@@ -770,7 +896,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t src = st0 + bx * kQBoxBytes + h * (kQBoxBytes / 2);
-            if (fused_gate)
+            if (fused)
               tma_store_3d(&tmap_out, src, h * kDHalf + bx * 64, 0, r);
             else
               tma_store_4d(&tmap_part, src, h * kDHalf + bx * 64, 0, r, s_idx);
@@ -779,8 +905,9 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         tma_store_commit();
       }
     }
+    }
     if (valid && (kStack ? i < 64 : half == 0)) {
-      if (fused_gate) {
+      if (fused) {
         p.lse[row_g] = lse_v;
       } else {
         const long long w = p.units ? slot : s_idx;
@@ -870,6 +997,22 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         mbar_arrive(oth_full(sx));
         if (it + 1 < ntiles) load_tile(it + 1);
       }
+    }
+  }
+
+  if constexpr (K::kHelp) {
+    if (K::is_helper(warp)) {
+      // ---------------------------------------------------------- epilogue helpers
+      // after the softmax warps have seen the last P V complete
+      named_bar_sync(kHandoffBarId, 256);
+      tc_fence_after();
+      const bool hl = (warp == K::kHelperLeaderWarp && lane == 0);
+      const EpilogueCtx ctx{&p, &tmap_out, &tmap_part, sptr, sbase, tmem, gate_full, kOffOwn, kOffQ, abort_flag,
+                            warp, lane, half, m_tile, r, s_idx, slot, Mq, fused};
+      store_boxes<kStack>(ctx, 2, 4, reinterpret_cast<const float*>(sptr + K::kOffRowScale)[(warp & 3) * 32 + lane],
+                          kHelperBarId, hl);
+      if (hl) tma_store_wait_read();  // SMEM stays valid until the stores have read it
+      __syncwarp();
     }
   }
 
