@@ -550,14 +550,12 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
               (kF8 || warp_wait(q_tma, 0, abort_flag, p.status));
     bool issued = false;
     auto zero_tail = [&](uint8_t* tile, int rows_valid) {
-      // rows no query row of this unit may see: zero them (pool slack may be NaN)
-      const int nrows = kTileN - rows_valid;
-      for (int idx = lane; idx < nrows * 4 * 8; idx += 32) {
-        const int c16 = idx & 7;
-        const int rr = (idx >> 3) % nrows;
-        const int b = (idx >> 3) / nrows;
-        *reinterpret_cast<uint4*>(tile + b * kBoxBytes + (rows_valid + rr) * 128 + c16 * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
+      // rows no query row of this unit may see: zero them (pool slack may be
+      // NaN, and P V would turn 0 * NaN into NaN); lane = 4 rows x 8 chunks
+      for (int rr = rows_valid + (lane >> 3); rr < kTileN; rr += 4) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          *reinterpret_cast<uint4*>(tile + b * kBoxBytes + rr * 128 + (lane & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
     };
     if (ok) tc_fence_after();
@@ -578,8 +576,10 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       }
       const int rows_valid = maxb_tile - (lo + it) * kTileN;
       if (rows_valid < kTileN) {
+        // the own half is V of P V; the other half feeds only scores (its
+        // slack columns are masked by selection), except in the stacked form
         zero_tail(sptr + kOffOwn + so * kHalfTileBytes, rows_valid);
-        zero_tail(sptr + kOffOth + sx * kHalfTileBytes, rows_valid);
+        if constexpr (kStack) zero_tail(sptr + kOffOth + sx * kHalfTileBytes, rows_valid);
         fence_proxy_async_smem();
         __syncwarp();
       }
