@@ -459,14 +459,23 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
   // ---- unit geometry (every thread derives the same values)
   const int t_first = (m_tile * kMTile) / p.H;
   const int t_last = min((m_tile * kMTile + kMTile - 1) / p.H, p.q_per_req - 1);
-  int maxb_tile = 0;
-  for (int t = t_first; t <= t_last; ++t)
-    maxb_tile = max(maxb_tile, load_bound(p, r * p.q_per_req + t));
+  // one pass over the request's bounds, with the out-of-range report after
+  // it (no side effect between the loads, so they overlap)
+  int maxb_tile = 0, maxb_req = 0;
+  {
+    const int cap = p.max_pages * kTileN;
+    bool bad = false;
+    for (int t = 0; t < p.q_per_req; ++t) {
+      const int b = __ldg(p.kv_bounds + r * p.q_per_req + t);
+      bad |= (b < 0) | (b > cap);
+      const int bc = min(max(b, 0), cap);
+      maxb_req = max(maxb_req, bc);
+      if (t >= t_first && t <= t_last) maxb_tile = max(maxb_tile, bc);
+    }
+    if (bad && p.status) atomicOr(p.status, SV_DEV_BAD_BOUND);
+  }
   int lo = plan_lo, hi = plan_hi;
   if (!p.units) {
-    int maxb_req = 0;
-    for (int t = 0; t < p.q_per_req; ++t)
-      maxb_req = max(maxb_req, load_bound(p, r * p.q_per_req + t));
     const int n_r = (maxb_req + kTileN - 1) / kTileN;
     lo = (int)((long long)s_idx * n_r / S);
     hi = (int)((long long)(s_idx + 1) * n_r / S);
