@@ -101,11 +101,17 @@ ATTENTION_SOURCES = ("mla_verify_decode.cu", "sv_ptx.cuh")
 
 
 def kernel_source_hash():
+    """Hash of the attention kernel's code: comments and whitespace are
+    dropped first, so that a comment edit keeps recorded counters valid."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verify_mla_gb300", "csrc")
     for fn in ATTENTION_SOURCES:
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + f.read())
+        with open(os.path.join(csrc, fn)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(fn.encode() + " ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -36,8 +36,9 @@
 //    the block table is applied per tile.  The own half (used by the scores
 //    and by P V) sits in a 3-stage ring; the other half (scores only) in a
 //    2-stage ring that is released as soon as the score MMA completes.  Pool
-//    slack beyond the tile's largest bound is zeroed in SMEM before use
-//    (0 * NaN safety).
+//    slack beyond the tile's largest bound is zeroed in the SMEM that P V
+//    reads (0 * NaN safety); in the score-only half it is masked by
+//    selection.
 //  * Epilogue.  One split: normalise, gate (the gate tile TMA-loaded into the
 //    query region after the last score MMA), bf16 out + lse.  Several
 //    splits: bf16 o/l and fp32 lse partials for the LSE merge.  The output
@@ -48,9 +49,13 @@
 //  * Work units.  Uniform splits decode the unit from blockIdx; the balanced
 //    plan (a one-CTA plan kernel, this grid its programmatic dependent) hands
 //    each CTA a unit of a list ordered longest first.
-//  * MMA issue.  Two issuing threads (scores; P V), so the tensor pipe is fed
-//    from two warps; each ring slot's descriptor is built once and a K step
-//    adds a constant to its low word.
+//  * MMA issue.  Separate issuing warps for the scores and for P V (and, in
+//    the long-unit instances, a second score warp for the odd tiles), so
+//    the tensor pipe is fed from several warps; each ring slot's descriptor
+//    is built once and a K step adds a constant to its low word.
+//  * Set-up.  One pass over the request's kv_bounds gives the tile's and the
+//    request's KV extent (an out-of-range bound is reported once, after the
+//    loads, so that they overlap).
 //  * Stacked instance (M <= 64 query rows, uniform splits).  One
 //    CTA holds both latent halves: rows 64..127 of its 128-row tile repeat
 //    rows 0..63 (the other query half is TMA-loaded twice), so score rows L
@@ -59,9 +64,11 @@
 //    tile's two latent halves, so lanes 0..63 of O accumulate latent
 //    0..255 and lanes 64..127 latent 256..511.  No second CTA recomputes
 //    the scores; the other-half ring is released after P V.
-//  * Roles: warp 0 TMA producer, warps 2-5 softmax and epilogue, three MMA
-//    issuers: warp 1 the even tiles' scores, warp 7 the odd tiles' scores,
-//    warp 6 P V (fp8-KV instance: warps 11, 10; its warps 6-9 convert).
+//  * Roles: warp 0 TMA producer, warps 2-5 softmax and epilogue, MMA
+//    issuers: warp 1 the (even tiles') scores, warp 6 P V and, in the
+//    long-unit instances, warp 7 the odd tiles' scores (fp8 KV: P V warp 10,
+//    odd-tile warp 11; its warps 6-9 convert the KV).  Template instances:
+//    KV format x one or two score warps x two-CTA or stacked form.
 //    Every wait is bounded; nothing traps.
 #include <cuda.h>
 #include <cudaTypedefs.h>
