@@ -142,7 +142,10 @@ const char* sv_status_string(sv_status s);
  * the sizes, never at device data): SV_SPLITS_BALANCED when R >= 2,
  * max_pages_per_req >= 64 and 2 * ceil(H*q_per_req/128) * R <= SMs (long
  * contexts whose units fit the SMs once), else a uniform count that fills the
- * SMs once with >= 2 KV tiles per split.
+ * SMs once with >= 2 KV tiles per split, counting one CTA per (request, row
+ * tile, split) when the stacked form will be taken for it (see
+ * sv_mla_verify_set_stacked; it also depends on that process-wide mode) and
+ * two otherwise.  The same count serves the fp8 entry point.
  * sv_mla_verify_workspace_bytes accepts any num_splits value mla_verify_decode
  * accepts except 0 (resolve it first). */
 int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pages_per_req);
