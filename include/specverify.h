@@ -92,7 +92,8 @@ const char* sv_status_string(sv_status s);
  * share the request's KV (row = t_local*H + h), processed as 128-row tiles;
  * each (row tile, KV split) runs on two CTAs, one per 256-column latent half
  * of the output.  With uniform splits and M <= 64, one CTA may hold both
- * halves instead (the "stacked" form, see sv_mla_verify_set_stacked).
+ * halves instead (the "stacked" form, see SV_FORM_* below); this call takes
+ * the automatic choice (SV_FORM_AUTO).
  *
  * Arguments (all device pointers unless stated):
  *   q_latent      bf16 [T][H][512], 16-byte aligned, contiguous.
@@ -138,39 +139,37 @@ const char* sv_status_string(sv_status s);
  *   stream        CUDA stream.
  * Returns SV_OK after enqueueing, or the first failed check.
  * ---------------------------------------------------------------------- */
-/* The num_splits that 0 resolves to on the current device (it only looks at
- * the sizes, never at device data): SV_SPLITS_BALANCED when R >= 2,
- * max_pages_per_req >= 64 and 2 * ceil(H*q_per_req/128) * R <= SMs (long
- * contexts whose units fit the SMs once), else a uniform count that fills the
- * SMs once with >= 2 KV tiles per split, counting one CTA per (request, row
- * tile, split) when the stacked form will be taken for it (see
- * sv_mla_verify_set_stacked; it also depends on that process-wide mode) and
- * two otherwise.  The same count serves the fp8 entry point.
- * sv_mla_verify_workspace_bytes accepts any num_splits value mla_verify_decode
- * accepts except 0 (resolve it first). */
-int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pages_per_req);
-size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits);
+/* The kernel form of the attention call, chosen per call (the `form`
+ * argument of mla_verify_decode_gated / _kv8 and sv_mla_verify_num_splits;
+ * mla_verify_decode uses SV_FORM_AUTO).  The stacked form runs requests of
+ * M = H*q_per_req <= 64 query rows with uniform splits on one CTA per
+ * (request, split): rows 64..127 of the CTA's 128-row MMA tile repeat rows
+ * 0..63, and the softmax weights P form a block-diagonal operand over the KV
+ * tile taken twice, so TMEM lanes 0..63 accumulate latent columns 0..255 and
+ * lanes 64..127 columns 256..511 (no second CTA recomputing the scores).
+ * The result is the same beyond rounding.
+ *   SV_FORM_AUTO      the stacked form when M <= 64, the splits are uniform
+ *                     and a unit holds at least 4 KV tiles
+ *                     (ceil(max_pages_per_req / S) >= 4); else two CTAs.
+ *   SV_FORM_TWO_CTA   always two CTAs per unit, one per latent half.
+ *   SV_FORM_STACKED   the stacked form whenever M <= 64 and the splits are
+ *                     uniform (else two CTAs).
+ * Any other value: SV_ERR_UNSUPPORTED (sv_mla_verify_num_splits returns 0). */
+#define SV_FORM_AUTO 0
+#define SV_FORM_TWO_CTA 1
+#define SV_FORM_STACKED 2
 
-/* The stacked form of the attention kernels, process-wide for every later
- * call; returns the previous mode, or -1 (nothing changed) for another value.
- * The stacked form runs requests of M = H*q_per_req <= 64 query rows with
- * uniform splits on one CTA per (request, split): rows 64..127 of the CTA's
- * 128-row MMA tile repeat rows 0..63, and the softmax weights P form a
- * block-diagonal operand over the KV tile taken twice, so TMEM lanes 0..63
- * accumulate latent columns 0..255 and lanes 64..127 columns 256..511 (no
- * second CTA recomputing the scores).  The result is the same beyond
- * rounding.
- *   SV_STACKED_OFF     never (two CTAs per unit, one per latent half);
- *   SV_STACKED_AUTO    (default) when a unit holds at least 4 KV tiles
- *                      (ceil(max_pages_per_req / S) >= 4);
- *   SV_STACKED_ALWAYS  whenever M <= 64.
- * The automatic split count (num_splits = 0) counts one CTA per unit for
- * the stacked form.  Meant for tests and tuning; not synchronised with
- * calls in flight on other threads. */
-#define SV_STACKED_OFF 0
-#define SV_STACKED_AUTO 1
-#define SV_STACKED_ALWAYS 2
-int sv_mla_verify_set_stacked(int mode);
+/* The num_splits that 0 resolves to on the current device for the given
+ * form (it only looks at the sizes, never at device data):
+ * SV_SPLITS_BALANCED when R >= 2, max_pages_per_req >= 64 and
+ * 2 * ceil(H*q_per_req/128) * R <= SMs (long contexts whose units fit the SMs
+ * once), else a uniform count that fills the SMs once with >= 2 KV tiles per
+ * split, counting one CTA per (request, row tile, split) when the stacked
+ * form will be taken for it and two otherwise.  The same count serves the
+ * fp8 entry point.  sv_mla_verify_workspace_bytes accepts any num_splits
+ * value mla_verify_decode accepts except 0 (resolve it first). */
+int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pages_per_req, int form);
+size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits);
 
 sv_status mla_verify_decode(const void* q_latent, const void* kv_pages, int num_pages,
                             int page_size, const int32_t* block_table, int R, int q_per_req,
@@ -189,15 +188,18 @@ sv_status mla_verify_decode(const void* q_latent, const void* kv_pages, int num_
  *   gate_dim == 512: gate bf16 [T][H][512], out = sigmoid(gate) * o
  *                    elementwise (exactly mla_verify_decode);
  *   gate_dim == 1:   gate bf16 [T][H], out[t][h][:] = sigmoid(gate[t][h]) * o.
- * Any other gate_dim returns SV_ERR_UNSUPPORTED.  All other arguments,
- * layouts and errors as mla_verify_decode; gate must be 16-byte aligned.
+ * Any other gate_dim returns SV_ERR_UNSUPPORTED.  `form` picks the kernel
+ * form (SV_FORM_*; num_splits = 0 then resolves to
+ * sv_mla_verify_num_splits(..., form)).  All other arguments, layouts and
+ * errors as mla_verify_decode; gate must be 16-byte aligned.
  * ---------------------------------------------------------------------- */
 sv_status mla_verify_decode_gated(const void* q_latent, const void* kv_pages, int num_pages,
                                   int page_size, const int32_t* block_table, int R,
                                   int q_per_req, int max_pages_per_req, const int32_t* kv_bounds,
                                   const void* gate, int gate_dim, int H, float softmax_scale,
-                                  int num_splits, void* workspace, size_t workspace_bytes,
-                                  void* out, float* lse, int32_t* status, sv_stream_t stream);
+                                  int num_splits, int form, void* workspace,
+                                  size_t workspace_bytes, void* out, float* lse, int32_t* status,
+                                  sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * mla_verify_decode_kv8
@@ -220,8 +222,9 @@ sv_status mla_verify_decode_kv8(const void* q_latent, const void* kv_pages_e4m3,
                                 int num_pages, int page_size, const int32_t* block_table, int R,
                                 int q_per_req, int max_pages_per_req, const int32_t* kv_bounds,
                                 const void* gate, int gate_dim, int H, float softmax_scale,
-                                int num_splits, void* workspace, size_t workspace_bytes,
-                                void* out, float* lse, int32_t* status, sv_stream_t stream);
+                                int num_splits, int form, void* workspace,
+                                size_t workspace_bytes, void* out, float* lse, int32_t* status,
+                                sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * mla_wuv_project

@@ -8,9 +8,9 @@ from .binding import (  # noqa: F401
     SV_DEV_BAD_BOUND,
     SV_DEV_BAD_PAGE,
     SV_DEV_TIMEOUT,
-    STACKED_ALWAYS,
-    STACKED_AUTO,
-    STACKED_OFF,
+    FORM_AUTO,
+    FORM_STACKED,
+    FORM_TWO_CTA,
     SV_SPLITS_BALANCED,
     SpecVerifyError,
     attention_workspace_bytes,
@@ -24,7 +24,6 @@ from .binding import (  # noqa: F401
     num_splits_for,
     sampled_workspace,
     sampled_workspace_bytes,
-    set_stacked,
     spec_verify_greedy,
     spec_verify_sampled,
     status_string,

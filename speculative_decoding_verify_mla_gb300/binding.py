@@ -25,7 +25,8 @@ SV_LATENT_DIM = 512
 SV_PAGE_SIZE = 64
 SV_MAX_SPLITS = 64
 SV_SPLITS_BALANCED = -1
-STACKED_OFF, STACKED_AUTO, STACKED_ALWAYS = 0, 1, 2
+# kernel form of the attention call (SV_FORM_*), chosen per call
+FORM_AUTO, FORM_TWO_CTA, FORM_STACKED = 0, 1, 2
 SV_DEV_BAD_PAGE = 0x1
 SV_DEV_BAD_BOUND = 0x2
 SV_DEV_TIMEOUT = 0x4
@@ -44,7 +45,6 @@ EXPORTED_SYMBOLS = (
     "mla_verify_decode_gated",
     "mla_wuv_project",
     "mla_verify_decode_kv8",
-    "sv_mla_verify_set_stacked",
 )
 
 _lib = None
@@ -71,10 +71,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib = ctypes.CDLL(path)
         lib.sv_status_string.argtypes = [_c_int]
         lib.sv_status_string.restype = ctypes.c_char_p
-        lib.sv_mla_verify_num_splits.argtypes = [_c_int, _c_int, _c_int, _c_int]
+        lib.sv_mla_verify_num_splits.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int]
         lib.sv_mla_verify_num_splits.restype = _c_int
-        lib.sv_mla_verify_set_stacked.argtypes = [_c_int]
-        lib.sv_mla_verify_set_stacked.restype = _c_int
         lib.sv_mla_verify_workspace_bytes.argtypes = [_c_int, _c_int, _c_int]
         lib.sv_mla_verify_workspace_bytes.restype = _c_size
         lib.mla_verify_decode.argtypes = [
@@ -102,15 +100,15 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.spec_verify_sampled.restype = _c_int
         lib.mla_verify_decode_gated.argtypes = [
             _c_void_p, _c_void_p, _c_int, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_void_p,
-            _c_void_p, _c_int, _c_int, _c_float, _c_int, _c_void_p, _c_size, _c_void_p, _c_void_p,
-            _c_void_p, _c_void_p]
+            _c_void_p, _c_int, _c_int, _c_float, _c_int, _c_int, _c_void_p, _c_size, _c_void_p,
+            _c_void_p, _c_void_p, _c_void_p]
         lib.mla_verify_decode_gated.restype = _c_int
         lib.mla_wuv_project.argtypes = [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_void_p,
                                         _c_void_p, _c_void_p]
         lib.mla_wuv_project.restype = _c_int
         lib.mla_verify_decode_kv8.argtypes = [
             _c_void_p, _c_void_p, _c_float, _c_int, _c_int, _c_void_p, _c_int, _c_int, _c_int,
-            _c_void_p, _c_void_p, _c_int, _c_int, _c_float, _c_int, _c_void_p, _c_size,
+            _c_void_p, _c_void_p, _c_int, _c_int, _c_float, _c_int, _c_int, _c_void_p, _c_size,
             _c_void_p, _c_void_p, _c_void_p, _c_void_p]
         lib.mla_verify_decode_kv8.restype = _c_int
         _lib = lib
@@ -139,18 +137,12 @@ def _check_status(func: str, code: int):
         raise SpecVerifyError(func, code)
 
 
-def num_splits_for(R: int, q_per_req: int, H: int, max_pages_per_req: int) -> int:
-    return int(load_library().sv_mla_verify_num_splits(R, q_per_req, H, max_pages_per_req))
-
-
-def set_stacked(mode: int) -> int:
-    """Mode of the stacked attention form (one CTA per unit for requests of
-    <= 64 query rows) for the process: STACKED_OFF, STACKED_AUTO (default)
-    or STACKED_ALWAYS; returns the previous mode."""
-    prev = int(load_library().sv_mla_verify_set_stacked(int(mode)))
-    if prev < 0:
-        raise ValueError(f"unknown stacked mode {mode}")
-    return prev
+def num_splits_for(R: int, q_per_req: int, H: int, max_pages_per_req: int, form: int = FORM_AUTO) -> int:
+    """The split count num_splits = 0 resolves to for this form."""
+    s = int(load_library().sv_mla_verify_num_splits(R, q_per_req, H, max_pages_per_req, int(form)))
+    if s == 0:
+        raise ValueError(f"unknown attention form {form}")
+    return s
 
 
 def attention_workspace_bytes(T: int, H: int, num_splits: int) -> int:
@@ -166,11 +158,13 @@ def mla_verify_decode(q_latent: torch.Tensor, kv_pages: torch.Tensor, block_tabl
                       softmax_scale: float, num_splits: int = 0,
                       workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
                       lse: torch.Tensor | None = None, status: torch.Tensor | None = None,
-                      kv_scale: float | None = None):
+                      kv_scale: float | None = None, form: int = FORM_AUTO):
     """Gated NoPE MLA verify attention.  Shapes: q_latent [T, H, 512] bf16,
     gate [T, H, 512] or [T, H] bf16, kv_pages [P, 64, 512] bf16 (or uint8 E4M3
     codes with kv_scale given), block_table [R, max_pages] int32, kv_bounds [T]
-    int32.  Returns (out [T, H, 512] bf16, lse [T, H] fp32)."""
+    int32.  ``form`` picks the kernel form (FORM_AUTO, FORM_TWO_CTA or
+    FORM_STACKED) for this call.  Returns (out [T, H, 512] bf16, lse [T, H]
+    fp32)."""
     lib = load_library()
     _check(q_latent.dim() == 3 and q_latent.shape[2] == SV_LATENT_DIM, "q_latent must be [T, H, 512]")
     T, H, _ = q_latent.shape
@@ -193,7 +187,7 @@ def mla_verify_decode(q_latent: torch.Tensor, kv_pages: torch.Tensor, block_tabl
     _check(T == R * q_per_req, "T must equal R * q_per_req")
     _check(tuple(kv_bounds.shape) == (T,), "kv_bounds must be [T]")
     if num_splits == 0:
-        num_splits = num_splits_for(R, q_per_req, H, max_pages)
+        num_splits = num_splits_for(R, q_per_req, H, max_pages, form)
     if out is None:
         out = torch.empty((T, H, SV_LATENT_DIM), dtype=torch.bfloat16, device=dev)
     if lse is None:
@@ -206,14 +200,14 @@ def mla_verify_decode(q_latent: torch.Tensor, kv_pages: torch.Tensor, block_tabl
         code = lib.mla_verify_decode_kv8(
             _ptr(q_latent), _ptr(kv_pages), float(kv_scale), int(kv_pages.shape[0]),
             int(kv_pages.shape[1]), _ptr(block_table), R, q_per_req, max_pages, _ptr(kv_bounds),
-            _ptr(gate), gate_dim, H, float(softmax_scale), int(num_splits), _ptr(workspace), ws_size,
-            _ptr(out), _ptr(lse), _ptr(status), _stream(dev))
+            _ptr(gate), gate_dim, H, float(softmax_scale), int(num_splits), int(form), _ptr(workspace),
+            ws_size, _ptr(out), _ptr(lse), _ptr(status), _stream(dev))
     else:
         code = lib.mla_verify_decode_gated(
             _ptr(q_latent), _ptr(kv_pages), int(kv_pages.shape[0]), int(kv_pages.shape[1]),
             _ptr(block_table), R, q_per_req, max_pages, _ptr(kv_bounds), _ptr(gate), gate_dim, H,
-            float(softmax_scale), int(num_splits), _ptr(workspace), ws_size, _ptr(out), _ptr(lse),
-            _ptr(status), _stream(dev))
+            float(softmax_scale), int(num_splits), int(form), _ptr(workspace), ws_size, _ptr(out),
+            _ptr(lse), _ptr(status), _stream(dev))
     _check_status("mla_verify_decode", code)
     return out, lse
 

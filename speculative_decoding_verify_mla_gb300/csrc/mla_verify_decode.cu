@@ -75,7 +75,6 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -1242,16 +1241,17 @@ bool device_setup(int* sm_count) {
 // tiles deep (a tile holds both ring slots until its P V completes), so it
 // pays only when a unit holds several tiles: measured on the C = 64 plain
 // decode batch (20 tiles per request) 47.5 us against 51.0 us for the
-// two-CTA form, and slower than it on 1-2 tile units.  Process-wide mode,
-// see sv_mla_verify_set_stacked.
+// two-CTA form, and slower than it on 1-2 tile units.  The caller picks the
+// form per call (SV_FORM_*); the automatic choice takes the stacked form for
+// units of at least kStackMinTiles tiles.
 constexpr int kStackMinTiles = 4;
-std::atomic<int> g_stack_mode{SV_STACKED_AUTO};
-inline int stack_mode() { return g_stack_mode.load(std::memory_order_relaxed); }
+inline bool valid_form(int form) {
+  return form == SV_FORM_AUTO || form == SV_FORM_TWO_CTA || form == SV_FORM_STACKED;
+}
 // Stacked form for units of ceil(max_pages / S) tiles?
-inline bool use_stack(long long Mq, long long max_pages, long long S) {
-  const int m = stack_mode();
-  if (Mq > 64 || m == SV_STACKED_OFF) return false;
-  return m == SV_STACKED_ALWAYS || (max_pages + S - 1) / S >= kStackMinTiles;
+inline bool use_stack(long long Mq, long long max_pages, long long S, int form) {
+  if (Mq > 64 || form == SV_FORM_TWO_CTA) return false;
+  return form == SV_FORM_STACKED || (max_pages + S - 1) / S >= kStackMinTiles;
 }
 
 // Splits: enough (request, row tile, split, latent half) CTAs to fill the SMs
@@ -1267,12 +1267,12 @@ int fill_splits(long long ctas_per_split, int max_pages, int sm_count) {
   if (s < 1) s = 1;
   return (int)s;
 }
-int auto_splits(int R, int q_per_req, int H, int max_pages, int sm_count) {
+int auto_splits(int R, int q_per_req, int H, int max_pages, int sm_count, int form) {
   const long long Mq = (long long)H * q_per_req;
   const long long n_mt = (Mq + kMTile - 1) / kMTile;
   // the stacked form if its own split count leaves it long enough units
   const int s_stack = fill_splits((long long)R * n_mt, max_pages, sm_count);
-  if (use_stack(Mq, max_pages, s_stack)) return s_stack;
+  if (use_stack(Mq, max_pages, s_stack, form)) return s_stack;
   return fill_splits(2ll * R * n_mt, max_pages, sm_count);
 }
 
@@ -1327,17 +1327,13 @@ size_t plan_workspace_bound(long long T, long long H, int sms) {
 // when the requests' row tiles fit the SMs once (so uniform splits would
 // leave SMs idle behind the longest request) and a request may hold at least
 // 64 tiles (4096 positions); otherwise uniform splits.
-extern "C" int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pages_per_req) {
+extern "C" int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pages_per_req, int form) {
+  if (!sv::valid_form(form)) return 0;
   const int sms = sv::current_sm_count();
   const long long n_mt = ((long long)H * q_per_req + sv::kMTile - 1) / sv::kMTile;
   if (R >= 2 && max_pages_per_req >= 64 && max_pages_per_req <= 0xFFFF && 2 * n_mt * R <= sms)
     return SV_SPLITS_BALANCED;
-  return sv::auto_splits(R, q_per_req, H, max_pages_per_req, sms);
-}
-
-extern "C" int sv_mla_verify_set_stacked(int mode) {
-  if (mode != SV_STACKED_OFF && mode != SV_STACKED_AUTO && mode != SV_STACKED_ALWAYS) return -1;
-  return sv::g_stack_mode.exchange(mode);
+  return sv::auto_splits(R, q_per_req, H, max_pages_per_req, sms, form);
 }
 
 extern "C" size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits) {
@@ -1357,11 +1353,12 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
                       int num_pages, int page_size, const int32_t* block_table, int R,
                       int q_per_req, int max_pages_per_req, const int32_t* kv_bounds,
                       const void* gate, int gate_dim, int H, float softmax_scale, int num_splits,
-                      void* workspace, size_t workspace_bytes, void* out, float* lse,
+                      int form, void* workspace, size_t workspace_bytes, void* out, float* lse,
                       int32_t* status, sv_stream_t stream) {
   if (R < 0 || q_per_req < 1 || H < 1 || max_pages_per_req < 0 || num_pages < 0)
     return SV_ERR_SHAPE;
   if (gate_dim != kD && gate_dim != 1) return SV_ERR_UNSUPPORTED;
+  if (!valid_form(form)) return SV_ERR_UNSUPPORTED;
   if (page_size != SV_PAGE_SIZE) return SV_ERR_UNSUPPORTED;
   if ((num_splits < 0 && num_splits != SV_SPLITS_BALANCED) || num_splits > SV_MAX_SPLITS)
     return SV_ERR_SHAPE;
@@ -1382,7 +1379,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   int sm_count = 0;
   if (!device_setup(&sm_count)) return SV_ERR_DEVICE;
   const int S = num_splits != 0 ? num_splits
-                                : sv_mla_verify_num_splits(R, q_per_req, H, max_pages_per_req);
+                                : sv_mla_verify_num_splits(R, q_per_req, H, max_pages_per_req, form);
   const bool balanced = (S == SV_SPLITS_BALANCED);
   const long long Mq_ll = (long long)H * q_per_req;
   const int n_mt = (int)((Mq_ll + kMTile - 1) / kMTile);
@@ -1411,7 +1408,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   const long long Mq = (long long)H * q_per_req;
   // stacked instance: requests of <= 64 query rows, uniform splits; its row
   // maps have 64-row boxes
-  const bool stack = !balanced && use_stack(Mq, max_pages_per_req, S);
+  const bool stack = !balanced && use_stack(Mq, max_pages_per_req, S, form);
   const int m_box = stack ? 64 : kMTile;
   CUtensorMap tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part;
   {
@@ -1536,13 +1533,13 @@ extern "C" sv_status mla_verify_decode_gated(const void* q_latent, const void* k
                                              const int32_t* block_table, int R, int q_per_req,
                                              int max_pages_per_req, const int32_t* kv_bounds,
                                              const void* gate, int gate_dim, int H,
-                                             float softmax_scale, int num_splits, void* workspace,
-                                             size_t workspace_bytes, void* out, float* lse,
-                                             int32_t* status, sv_stream_t stream) {
+                                             float softmax_scale, int num_splits, int form,
+                                             void* workspace, size_t workspace_bytes, void* out,
+                                             float* lse, int32_t* status, sv_stream_t stream) {
   return sv::verify_impl(q_latent, kv_pages, false, 1.0f, num_pages, page_size, block_table, R,
                          q_per_req, max_pages_per_req, kv_bounds, gate, gate_dim, H,
-                         softmax_scale, num_splits, workspace, workspace_bytes, out, lse, status,
-                         stream);
+                         softmax_scale, num_splits, form, workspace, workspace_bytes, out, lse,
+                         status, stream);
 }
 
 extern "C" sv_status mla_verify_decode_kv8(const void* q_latent, const void* kv_pages_e4m3,
@@ -1550,12 +1547,12 @@ extern "C" sv_status mla_verify_decode_kv8(const void* q_latent, const void* kv_
                                            const int32_t* block_table, int R, int q_per_req,
                                            int max_pages_per_req, const int32_t* kv_bounds,
                                            const void* gate, int gate_dim, int H,
-                                           float softmax_scale, int num_splits, void* workspace,
-                                           size_t workspace_bytes, void* out, float* lse,
-                                           int32_t* status, sv_stream_t stream) {
+                                           float softmax_scale, int num_splits, int form,
+                                           void* workspace, size_t workspace_bytes, void* out,
+                                           float* lse, int32_t* status, sv_stream_t stream) {
   return sv::verify_impl(q_latent, kv_pages_e4m3, true, kv_scale, num_pages, page_size,
                          block_table, R, q_per_req, max_pages_per_req, kv_bounds, gate, gate_dim,
-                         H, softmax_scale, num_splits, workspace, workspace_bytes, out, lse,
+                         H, softmax_scale, num_splits, form, workspace, workspace_bytes, out, lse,
                          status, stream);
 }
 
@@ -1568,8 +1565,8 @@ extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_page
                                        int32_t* status, sv_stream_t stream) {
   return mla_verify_decode_gated(q_latent, kv_pages, num_pages, page_size, block_table, R,
                                  q_per_req, max_pages_per_req, kv_bounds, gate, SV_LATENT_DIM, H,
-                                 softmax_scale, num_splits, workspace, workspace_bytes, out, lse,
-                                 status, stream);
+                                 softmax_scale, num_splits, SV_FORM_AUTO, workspace,
+                                 workspace_bytes, out, lse, status, stream);
 }
 
 extern "C" const char* sv_status_string(sv_status s) {

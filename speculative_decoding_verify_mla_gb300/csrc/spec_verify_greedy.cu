@@ -18,6 +18,8 @@
 // (a zero slot means every draft matched), then writes accepted / next token /
 // trimmed kv_lens, and leaves the ticket and all slots zero again.  Nothing
 // waits on another CTA.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -176,38 +178,70 @@ extern "C" size_t sv_greedy_workspace_bytes(int T, int V) {
   return sv::kGreedyHeader + (size_t)T * sizeof(unsigned long long) + (size_t)T * sizeof(int);
 }
 
+namespace sv {
+namespace {
+
+// Host-side checks of everything but the workspace, shared by both greedy
+// entry points so that a failed check enqueues nothing in either.  SV_OK with
+// *empty = true: T == 0, nothing to do.
+sv_status greedy_check(const float* logits, int T, int V, int R, int k, const int32_t* draft_tokens,
+                       const int32_t* kv_lens_in, const int32_t* argmax_ids, const int32_t* accepted,
+                       const int32_t* next_tokens, const int32_t* kv_lens_out, bool* empty) {
+  *empty = false;
+  if (T < 0 || R < 0 || k < 0) return SV_ERR_SHAPE;
+  if ((long long)R * (k + 1) != (long long)T) return SV_ERR_SHAPE;
+  if (T == 0) {
+    *empty = true;
+    return SV_OK;
+  }
+  if (V < 1) return SV_ERR_SHAPE;
+  if ((long long)V > 0x7FFFFFFFll - 32768) return SV_ERR_SHAPE;
+  if (!logits || !kv_lens_in || !argmax_ids || !accepted || !next_tokens || !kv_lens_out)
+    return SV_ERR_NULL;
+  if (k > 0 && !draft_tokens) return SV_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(logits) & 3u) return SV_ERR_ALIGN;
+  const int chunk = greedy_chunk(T, V);
+  const long long nchunks = (V + (long long)chunk - 1) / chunk;
+  if ((long long)T * nchunks > 0x7FFFFFFFll) return SV_ERR_SHAPE;
+  return SV_OK;
+}
+
+// The launch itself, after every check has passed (workspace: zero-filled,
+// 256-byte aligned, at least sv_greedy_workspace_bytes(T, V) bytes).
+sv_status greedy_launch(const float* logits, int T, int V, int R, int k, const int32_t* draft_tokens,
+                        const int32_t* kv_lens_in, int32_t* argmax_ids, int32_t* accepted,
+                        int32_t* next_tokens, int32_t* kv_lens_out, void* workspace, cudaStream_t stream) {
+  const int chunk = greedy_chunk(T, V);
+  const int nchunks = (int)((V + (long long)chunk - 1) / chunk);
+  const long long blocks = (long long)T * nchunks;
+  const bool vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
+  auto* ticket = reinterpret_cast<unsigned int*>(workspace);
+  auto* row_key = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + kGreedyHeader);
+  auto* mis = reinterpret_cast<int*>(row_key + T);
+  greedy_verify_kernel<<<(unsigned)blocks, kGreedyThreads, 0, stream>>>(
+      logits, T, V, R, k, chunk, nchunks, vec4, draft_tokens, kv_lens_in, argmax_ids, accepted,
+      next_tokens, kv_lens_out, ticket, row_key, mis);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace sv
+
 extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R, int k,
                                         const int32_t* draft_tokens, const int32_t* kv_lens_in,
                                         int32_t* argmax_ids, int32_t* accepted,
                                         int32_t* next_tokens, int32_t* kv_lens_out,
                                         void* workspace, size_t workspace_bytes,
                                         sv_stream_t stream) {
-  if (T < 0 || R < 0 || k < 0) return SV_ERR_SHAPE;
-  if ((long long)R * (k + 1) != (long long)T) return SV_ERR_SHAPE;
-  if (T == 0) return SV_OK;
-  if (V < 1) return SV_ERR_SHAPE;
-  if ((long long)V > 0x7FFFFFFFll - 32768) return SV_ERR_SHAPE;
-  if (!logits || !kv_lens_in || !argmax_ids || !accepted || !next_tokens || !kv_lens_out ||
-      !workspace)
-    return SV_ERR_NULL;
-  if (k > 0 && !draft_tokens) return SV_ERR_NULL;
-  if ((reinterpret_cast<uintptr_t>(logits) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return SV_ERR_ALIGN;
+  bool empty = false;
+  const sv_status st = sv::greedy_check(logits, T, V, R, k, draft_tokens, kv_lens_in, argmax_ids,
+                                        accepted, next_tokens, kv_lens_out, &empty);
+  if (st != SV_OK || empty) return st;
+  if (!workspace) return SV_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return SV_ERR_ALIGN;
   if (workspace_bytes < sv_greedy_workspace_bytes(T, V)) return SV_ERR_WORKSPACE;
-  const int chunk = sv::greedy_chunk(T, V);
-  const int nchunks = (int)((V + (long long)chunk - 1) / chunk);
-  const long long blocks = (long long)T * nchunks;
-  if (blocks > 0x7FFFFFFFll) return SV_ERR_SHAPE;
-  const bool vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
-  auto* ticket = reinterpret_cast<unsigned int*>(workspace);
-  auto* row_key = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) +
-                                                        sv::kGreedyHeader);
-  auto* mis = reinterpret_cast<int*>(row_key + T);
-  sv::greedy_verify_kernel<<<(unsigned)blocks, sv::kGreedyThreads, 0,
-                             reinterpret_cast<cudaStream_t>(stream)>>>(
-      logits, T, V, R, k, chunk, nchunks, vec4, draft_tokens, kv_lens_in, argmax_ids, accepted,
-      next_tokens, kv_lens_out, ticket, row_key, mis);
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_LAUNCH;
+  return sv::greedy_launch(logits, T, V, R, k, draft_tokens, kv_lens_in, argmax_ids, accepted,
+                           next_tokens, kv_lens_out, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -225,14 +259,19 @@ extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R
 //  * The array holds kNoAllocScratchBytes (512 KiB) on every GPU that loads
 //    this library, until the process exits.  A problem whose workspace
 //    (sv_greedy_workspace_bytes(T, V)) is larger is rejected with
-//    SV_ERR_WORKSPACE before anything is enqueued.
+//    SV_ERR_WORKSPACE; every argument is checked before anything is
+//    enqueued.
 //  * Every call shares the one array: calls whose kernels could overlap on the
 //    GPU (different streams without ordering, or several host threads) race
 //    on it and give wrong results.  Calls issued in order on one stream are
 //    fine.
-//  * The first call on a device looks up the array's device address
-//    (cudaGetSymbolAddress) with that device current and caches it; make that
-//    first call before any stream capture begins.
+//  * The first call on a device (per CUDA context) looks up the array's
+//    device address (cudaGetSymbolAddress) with that device current and
+//    caches it with the context; a call from another context looks it up
+//    again.  Make the first call before any stream capture begins.  A
+//    cudaDeviceReset of the device may keep the context handle while the
+//    array moves, so this entry point must not be used on a device after the
+//    process has reset it.
 //  * The counter, keys and slots must start at zero: each call clears the
 //    part it uses with a cudaMemsetAsync on the same stream before the kernel
 //    runs (every call also leaves them zero).
@@ -243,23 +282,46 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = 512 * 1024;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+PFN_cuCtxGetCurrent_v4000 get_ctx_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
+  });
+  return fn;
+}
+
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[64];
+CUcontext g_noalloc_ctx[64];
 
-// Device address of g_noalloc_scratch on the current device (nullptr on failure).
+// Device address of g_noalloc_scratch on the current device and context
+// (nullptr on failure).
 void* noalloc_scratch_for_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  auto ctx_fn = get_ctx_fn();
+  if (!ctx_fn) return nullptr;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    g_noalloc_ptr[dev] = p;
+  CUcontext ctx = nullptr;
+  if (ctx_fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  if (ctx != nullptr && g_noalloc_ptr[dev] && g_noalloc_ctx[dev] == ctx) return g_noalloc_ptr[dev];
+  // first call on this device or another context: the runtime call below
+  // also makes the device's primary context current when none is
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return nullptr;
   }
-  return g_noalloc_ptr[dev];
+  if (ctx == nullptr && (ctx_fn(&ctx) != CUDA_SUCCESS || ctx == nullptr)) return nullptr;
+  g_noalloc_ptr[dev] = p;
+  g_noalloc_ctx[dev] = ctx;
+  return p;
 }
 
 }  // namespace
@@ -270,18 +332,19 @@ extern "C" sv_status spec_verify_greedy_noalloc(const float* logits, int T, int 
                                                 const int32_t* kv_lens_in, int32_t* argmax_ids,
                                                 int32_t* accepted, int32_t* next_tokens,
                                                 int32_t* kv_lens_out, sv_stream_t stream) {
-  if (T < 0 || R < 0 || k < 0) return SV_ERR_SHAPE;
-  if ((long long)R * (k + 1) != (long long)T) return SV_ERR_SHAPE;
-  if (T == 0) return SV_OK;
-  if (V < 1) return SV_ERR_SHAPE;
+  bool empty = false;
+  const sv_status st = sv::greedy_check(logits, T, V, R, k, draft_tokens, kv_lens_in, argmax_ids,
+                                        accepted, next_tokens, kv_lens_out, &empty);
+  if (st != SV_OK || empty) return st;
   const size_t need = sv_greedy_workspace_bytes(T, V);
   if (need > sv::kNoAllocScratchBytes) return SV_ERR_WORKSPACE;
   void* scratch = sv::noalloc_scratch_for_current_device();
   if (!scratch) return SV_ERR_DEVICE;
-  if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+  const cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, need, st_) != cudaSuccess) {
     cudaGetLastError();
     return SV_ERR_LAUNCH;
   }
-  return spec_verify_greedy(logits, T, V, R, k, draft_tokens, kv_lens_in, argmax_ids, accepted,
-                            next_tokens, kv_lens_out, scratch, sv::kNoAllocScratchBytes, stream);
+  return sv::greedy_launch(logits, T, V, R, k, draft_tokens, kv_lens_in, argmax_ids, accepted,
+                           next_tokens, kv_lens_out, scratch, st_);
 }

@@ -151,34 +151,30 @@ def test_auto_split_choice(lib):
     assert num_splits_for(32, 5, 64, 24) >= 1      # short contexts: uniform splits
 
 
-def test_stacked_switch(lib):
-    """The stacked-form mode is process-wide, returns the previous mode,
-    rejects unknown modes and changes the automatic split count for requests
-    of <= 64 query rows (one CTA per unit instead of two, when the units
-    stay >= 4 tiles long); larger requests are unaffected."""
+def test_form_is_per_call(lib):
+    """The kernel form is an argument of each call (no process-wide state):
+    the split query takes it, unknown forms are rejected, and the stacked
+    form changes the automatic split count for requests of <= 64 query rows
+    (one CTA per unit instead of two, when the units stay >= 4 tiles long);
+    larger requests are unaffected."""
     import speculative_decoding_verify_mla_gb300 as sv
     sms = 152  # no device here: the library's fallback SM count
-    prev = sv.set_stacked(sv.STACKED_AUTO)
-    try:
-        assert sv.set_stacked(sv.STACKED_AUTO) == sv.STACKED_AUTO
-        auto = sv.num_splits_for(64, 1, 64, 24)
-        short = sv.num_splits_for(2, 4, 8, 2)
-        wide_auto = sv.num_splits_for(1, 8, 64, 24)
-        assert sv.set_stacked(sv.STACKED_ALWAYS) == sv.STACKED_AUTO
-        always_short = sv.num_splits_for(2, 4, 8, 8)
-        assert sv.set_stacked(sv.STACKED_OFF) == sv.STACKED_ALWAYS
-        off = sv.num_splits_for(64, 1, 64, 24)
-        off_short = sv.num_splits_for(2, 4, 8, 8)
-        wide_off = sv.num_splits_for(1, 8, 64, 24)
-        with pytest.raises(ValueError):
-            sv.set_stacked(7)
-        assert sv.set_stacked(sv.STACKED_OFF) == sv.STACKED_OFF
-    finally:
-        sv.set_stacked(prev)
+    auto = sv.num_splits_for(64, 1, 64, 24, sv.FORM_AUTO)
+    short = sv.num_splits_for(2, 4, 8, 2, sv.FORM_AUTO)
+    always_short = sv.num_splits_for(2, 4, 8, 8, sv.FORM_STACKED)
+    off = sv.num_splits_for(64, 1, 64, 24, sv.FORM_TWO_CTA)
+    off_short = sv.num_splits_for(2, 4, 8, 8, sv.FORM_TWO_CTA)
+    wide_auto = sv.num_splits_for(1, 8, 64, 24, sv.FORM_AUTO)
+    wide_off = sv.num_splits_for(1, 8, 64, 24, sv.FORM_TWO_CTA)
     assert auto == min(sms // 64, 24 // 2) and off == min(sms // 128, 24 // 2)
     assert short == 1                              # 2-page units: the two-CTA form, 1 split
     assert always_short == 4 and off_short == 4    # 8 pages: min(SMs / CTAs per split, 8 / 2)
     assert wide_auto == wide_off
+    # the calls' answers do not depend on the order they were made in
+    assert sv.num_splits_for(64, 1, 64, 24, sv.FORM_AUTO) == auto
+    with pytest.raises(ValueError):
+        sv.num_splits_for(64, 1, 64, 24, 7)
+    assert lib.sv_mla_verify_num_splits(64, 1, 64, 24, -1) == 0
 
 
 def test_gated_and_wuv_host_checks(lib):
@@ -191,9 +187,11 @@ def test_gated_and_wuv_host_checks(lib):
         a.update(kw)
         return lib.mla_verify_decode_gated(a["q"], a["kv"], a["num_pages"], a["page_size"], a["bt"], a["R"],
                                            a["qpr"], a["maxp"], a["bounds"], a["gate"], gate_dim, a["H"],
-                                           ctypes.c_float(a["scale"]), a["splits"], a["ws"], a["ws_bytes"],
-                                           a["out"], a["lse"], a["status"], a["stream"])
+                                           ctypes.c_float(a["scale"]), a["splits"], a.get("form", 0), a["ws"],
+                                           a["ws_bytes"], a["out"], a["lse"], a["status"], a["stream"])
     assert gated(7) == 5          # gate_dim must be 512 or 1
+    assert gated(1, form=3) == 5  # unknown kernel form
+    assert gated(1, form=-1) == 5
     assert gated(1, R=0) == 0
     assert gated(1, q=None) == 1
     f = lib.mla_wuv_project
@@ -207,7 +205,7 @@ def test_gated_and_wuv_host_checks(lib):
 def test_kv8_host_checks(lib):
     f = lib.mla_verify_decode_kv8
     fl = ctypes.c_float
-    base = [1 << 12, 1 << 12, fl(0.5), 4, 64, 1 << 12, 2, 4, 2, 1 << 12, 1 << 12, 512, 8, fl(0.1), 1,
+    base = [1 << 12, 1 << 12, fl(0.5), 4, 64, 1 << 12, 2, 4, 2, 1 << 12, 1 << 12, 512, 8, fl(0.1), 1, 0,
             None, 0, 1 << 12, 1 << 12, None, None]
     a = list(base); a[2] = fl(0.0)
     assert f(*a) == 2            # kv_scale must be > 0
@@ -219,3 +217,5 @@ def test_kv8_host_checks(lib):
     assert f(*a) == 1
     a = list(base); a[6] = 0
     assert f(*a) == 0            # no requests
+    a = list(base); a[15] = 9
+    assert f(*a) == 5            # unknown kernel form

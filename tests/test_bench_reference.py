@@ -1,5 +1,6 @@
 """bench.py's reference arm on the CPU: it times the float64 oracle on the
-bench workload and prints one JSON line with the contract's keys."""
+bench workload (a bounded, rotating sample of its requests per step, scaled
+to the whole batch) and prints one JSON line with the contract's keys."""
 import json
 import os
 import subprocess
@@ -20,4 +21,5 @@ def test_reference_arm_json_line():
     base = line["cpu_baseline"]
     assert base["kind"] == "oracle" and base["cores"] >= 1 and base["value"] == line["value"] and base["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
-    assert line["config"]["workload"].startswith("c1")
+    assert line["config"]["workload"].startswith("c4")
+    assert "requests each step" in base["sample"] and "median of 3 steps" in base["sample"]

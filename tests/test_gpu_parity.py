@@ -165,29 +165,20 @@ def test_attention_configs(sv, name):
     check_attention(out, lse, ref_o, ref_l, label=name)
 
 
-def test_attention_c4_sampled(sv):
-    """Full-size long-context workload on the GPU; the oracle checks sampled
-    tokens one by one (every zero-bound token plus whole straddling groups)."""
+def test_attention_c4_full(sv):
+    """The full-size long-context workload (16 requests, contexts 8K-32K,
+    straddling groups, 10% zero bounds; the balanced split plan cuts every
+    request into pieces) against the oracle on every token and head."""
     inp = inputs_for("c4")
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     out, lse = run_attention(sv, inp, status=status)
     assert int(status.item()) == 0
-    k1 = inp["k"] + 1
-    L = inp["kv_lens_in"]
-    straddle = [r for r in range(inp["R"]) if 1 <= L[r] % 64 <= inp["k"]][:2]
-    toks = sorted(set(inp["zero_bound_tokens"].tolist()) | {r * k1 + t for r in straddle for t in range(k1)})
-    ref_o = np.zeros((len(toks), inp["H"], 512))
-    ref_l = np.zeros((len(toks), inp["H"]))
-    for n, t in enumerate(toks):
-        r = t // k1
-        o1, l1 = oracle.ref_verify_attention(inp["q_bits"][t:t + 1], inp["kv_bits"], inp["block_table"][r:r + 1],
-                                             inp["kv_bounds"][t:t + 1], inp["gate_bits"][t:t + 1], 1,
-                                             inp["softmax_scale"])
-        ref_o[n], ref_l[n] = o1[0], l1[0]
-    check_attention(out, lse, ref_o, ref_l, rows=np.array(toks), label="c4 sampled")
-    # properties that hold at any size: finite everywhere a bound is > 0
+    ref_o, ref_l = oracle_attention(inp)
+    check_attention(out, lse, ref_o, ref_l, label="c4 full")
+    # the zero-bound tokens give exactly (-inf, 0), every other row is finite
     l = to_f64(lse)
     pos = inp["kv_bounds"] > 0
+    assert (~pos).sum() == len(inp["zero_bound_tokens"]) > 0
     assert np.all(np.isfinite(l[pos])) and np.all(l[~pos] == -np.inf)
 
 
@@ -284,13 +275,9 @@ def test_fold_equals_single_token_decode(sv):
     bt1 = torch.repeat_interleave(d["block_table"], k1, dim=0).contiguous()
     # one-token requests have 64 query rows: keep them on the same (two-CTA)
     # form as the verify groups
-    prev = sv.set_stacked(sv.STACKED_OFF)
-    try:
-        out1, lse1 = sv.mla_verify_decode(d["q"], d["kv"], bt1, d["kv_bounds"], d["gate"], 1,
-                                          inp["softmax_scale"], num_splits=1)
-        torch.cuda.synchronize()
-    finally:
-        sv.set_stacked(prev)
+    out1, lse1 = sv.mla_verify_decode(d["q"], d["kv"], bt1, d["kv_bounds"], d["gate"], 1,
+                                      inp["softmax_scale"], num_splits=1, form=sv.FORM_TWO_CTA)
+    torch.cuda.synchronize()
     assert torch.equal(out, out1)
     assert torch.equal(lse, lse1)
 

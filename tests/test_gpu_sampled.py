@@ -4,7 +4,10 @@ oracle, called through the C ABI.
 The kernels take their decisions in fp32, the oracle in float64.  A decision
 whose oracle margin is wider than the fp32 error bound must come out the same;
 one inside it may go either way, and the test then checks that the GPU's
-choice is one of the valid ones:
+choice is one of the valid ones.  An ambiguous acceptance does not exempt its
+request: the oracle is run again on that request with the decision forced to
+the GPU's choice (uniform 0 forces an acceptance, +inf a rejection), so every
+other decision, the trim and the draw that follow are still compared.
 * acceptance: relative gap |u q - p| / max(u q, p) below ACCEPT_TOL (fp32
   products and the ex2-based softmax carry ~1e-6 relative error);
 * draw: the GPU's id v must have positive weight and a CDF step
@@ -48,6 +51,29 @@ def run_gpu(sv, inp, temperature=None):
     return [r.cpu().numpy().astype(np.int64) for r in res]
 
 
+def _oracle_following_gpu(inp, r, ga_r, temp):
+    """The oracle on request r alone, with every acceptance test whose margin
+    is inside ACCEPT_TOL forced to the decision the GPU took there (the GPU
+    accepted drafts 0..ga_r-1 and rejected draft ga_r).  Returns (accepted,
+    next token, detail, number of forced decisions)."""
+    k = inp["k"]
+    rows = slice(r * (k + 1), (r + 1) * (k + 1))
+    u = np.asarray(inp["uniforms"][r:r + 1], dtype=np.float64).copy()
+    forced = set()
+    while True:
+        a, nxt, _, info = oracle.ref_sampled_verify(inp["logits"][rows], inp["draft_tokens"][r:r + 1],
+                                                    inp["draft_probs"][r:r + 1], u, inp["kv_lens_in"][r:r + 1],
+                                                    k, temp, detail=True)
+        amb = [j for j, g in enumerate(info[0]["accept_gaps"]) if g < ACCEPT_TOL and j not in forced]
+        if not amb:
+            return int(a[0]), int(nxt[0]), info[0], len(forced)
+        j = amb[0]
+        assert j <= ga_r, (f"request {r}: the GPU rejected draft {ga_r} although the oracle's decision "
+                           "there is clear")
+        u[0, j] = 0.0 if j < ga_r else np.inf
+        forced.add(j)
+
+
 def check_sampled(inp, got, temperature=None, max_ambiguous_frac=0.1):
     temp = inp["temperature"] if temperature is None else temperature
     k = inp["k"]
@@ -61,20 +87,23 @@ def check_sampled(inp, got, temperature=None, max_ambiguous_frac=0.1):
     draws_checked = 0
     for r in range(R):
         gaps = info[r]["accept_gaps"]
+        a_r, n_r, info_r = a[r], nxt[r], info[r]
         if gaps and min(gaps) < ACCEPT_TOL:
             ambiguous += 1
-            continue
-        assert ga[r] == a[r], f"request {r}: accepted {ga[r]} vs oracle {a[r]}"
+            a_r, n_r, info_r, n_forced = _oracle_following_gpu(inp, r, int(ga[r]), temp)
+            assert n_forced >= 1
+        assert ga[r] == a_r, f"request {r}: accepted {ga[r]} vs oracle {a_r}"
         draws_checked += 1
-        if gn[r] == nxt[r]:
+        if gn[r] == n_r:
             continue
-        assert info[r]["draw_gap"] < DRAW_TOL, (
-            f"request {r}: drew {gn[r]} vs oracle {nxt[r]} although the oracle's CDF margin is "
-            f"{info[r]['draw_gap']:.2e} of the total")
+        assert info_r["draw_gap"] < DRAW_TOL, (
+            f"request {r}: drew {gn[r]} vs oracle {n_r} although the oracle's CDF margin is "
+            f"{info_r['draw_gap']:.2e} of the total")
         v = int(gn[r])
-        w, c, tgt = info[r]["weights"], info[r]["cdf"], info[r]["target"]
+        w, c, tgt = info_r["weights"], info_r["cdf"], info_r["target"]
         W = c[-1]
         lo = c[v - 1] if v > 0 else 0.0
+        assert 0 <= v < len(w), f"request {r}: drew id {v} outside the vocabulary"
         assert w[v] > 0, f"request {r}: drew id {v} of zero weight"
         assert lo - DRAW_TOL * W <= tgt <= c[v] + DRAW_TOL * W, f"request {r}: id {v} outside the CDF step"
     assert ambiguous <= max(1, int(max_ambiguous_frac * R)), f"{ambiguous} ambiguous requests of {R}"

@@ -1,6 +1,7 @@
 """GPU parity of the stacked attention form (requests of at most 64 query
 rows on one CTA that holds both latent halves) against the float64 oracle,
-with the form switched on and off on the same inputs (C ABI calls)."""
+with the form chosen per call (forced on, forced off, automatic) on the same
+inputs (C ABI calls)."""
 import numpy as np
 import pytest
 import torch
@@ -23,30 +24,22 @@ def sv():
     return m
 
 
-class stacked:
-    """Context manager: the stacked form always (on) or never (off), or the
-    given mode, restored afterwards."""
-
-    def __init__(self, sv, on):
-        self.sv = sv
-        self.mode = on if isinstance(on, int) and not isinstance(on, bool) else \
-            (sv.STACKED_ALWAYS if on else sv.STACKED_OFF)
-
-    def __enter__(self):
-        self.prev = self.sv.set_stacked(self.mode)
-
-    def __exit__(self, *exc):
-        self.sv.set_stacked(self.prev)
+def form_of(sv, on):
+    """The per-call kernel form: stacked (True), two CTAs (False), or the
+    given SV_FORM_* value."""
+    if isinstance(on, bool):
+        return sv.FORM_STACKED if on else sv.FORM_TWO_CTA
+    return on
 
 
-def _attention(sv, inp, splits, bounds=None, kv_bits=None, gate_bits=None):
+def _attention(sv, inp, splits, bounds=None, kv_bits=None, gate_bits=None, form=0):
     d = device_inputs(inp, DEV)
     kv = d["kv"] if kv_bits is None else bf16_tensor(kv_bits, DEV)
     kb = d["kv_bounds"] if bounds is None else i32(bounds, DEV)
     gate = d["gate"] if gate_bits is None else bf16_tensor(gate_bits, DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     out, lse = sv.mla_verify_decode(d["q"], kv, d["block_table"], kb, gate, inp["k"] + 1, inp["softmax_scale"],
-                                    num_splits=splits, status=status)
+                                    num_splits=splits, status=status, form=form)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     return out, lse
@@ -72,10 +65,9 @@ def test_stacked_matches_oracle(sv, H, k, lens, on):
     cfg = small_config("c0", R=len(lens), k=k, H=H, kv_lens=lens, shuffled=True, vocab=64)
     inp = make_inputs(cfg, seed=11)
     ref_o, ref_l = _oracle(inp)
-    with stacked(sv, on):
-        for splits in (1, 2, 5, 0):
-            out, lse = _attention(sv, inp, splits)
-            check_attention(out, lse, ref_o, ref_l, label=f"stacked={on} H={H} k={k} splits={splits}")
+    for splits in (1, 2, 5, 0):
+        out, lse = _attention(sv, inp, splits, form=form_of(sv, on))
+        check_attention(out, lse, ref_o, ref_l, label=f"stacked={on} H={H} k={k} splits={splits}")
 
 
 def test_stacked_zero_bounds_nan_slack_headwise_gate(sv):
@@ -94,12 +86,11 @@ def test_stacked_zero_bounds_nan_slack_headwise_gate(sv):
     ref_o, ref_l = _oracle(inp, bounds=bounds, kv_bits=kv)
     g_head = np.ascontiguousarray(inp["gate_bits"][:, :, 0])
     ref_oh, ref_lh = _oracle(inp, bounds=bounds, kv_bits=kv, gate_bits=g_head)
-    with stacked(sv, True):
-        for splits in (1, 4):
-            out, lse = _attention(sv, inp, splits, bounds=bounds, kv_bits=kv)
-            check_attention(out, lse, ref_o, ref_l, label=f"zero bounds + nan slack, splits={splits}")
-            out, lse = _attention(sv, inp, splits, bounds=bounds, kv_bits=kv, gate_bits=g_head)
-            check_attention(out, lse, ref_oh, ref_lh, label=f"head-wise gate, splits={splits}")
+    for splits in (1, 4):
+        out, lse = _attention(sv, inp, splits, bounds=bounds, kv_bits=kv, form=sv.FORM_STACKED)
+        check_attention(out, lse, ref_o, ref_l, label=f"zero bounds + nan slack, splits={splits}")
+        out, lse = _attention(sv, inp, splits, bounds=bounds, kv_bits=kv, gate_bits=g_head, form=sv.FORM_STACKED)
+        check_attention(out, lse, ref_oh, ref_lh, label=f"head-wise gate, splits={splits}")
 
 
 def test_stacked_partials_layout(sv):
@@ -111,10 +102,9 @@ def test_stacked_partials_layout(sv):
     d = device_inputs(inp, DEV)
     T, H = inp["T"], inp["H"]
     ws = torch.empty(sv.attention_workspace_bytes(T, H, S), dtype=torch.uint8, device=DEV)
-    with stacked(sv, True):
-        sv.mla_verify_decode(d["q"], d["kv"], d["block_table"], d["kv_bounds"], d["gate"], 1,
-                             inp["softmax_scale"], num_splits=S, workspace=ws)
-        torch.cuda.synchronize()
+    sv.mla_verify_decode(d["q"], d["kv"], d["block_table"], d["kv_bounds"], d["gate"], 1,
+                         inp["softmax_scale"], num_splits=S, workspace=ws, form=sv.FORM_STACKED)
+    torch.cuda.synchronize()
     n_o = S * T * H * 512
     part_o = ws[:2 * n_o].view(torch.bfloat16).view(S, T, H, 512)
     part_lse = ws[2 * n_o:2 * n_o + 4 * S * T * H].view(torch.float32).view(S, T, H)
@@ -140,10 +130,8 @@ def test_stacked_equals_two_cta_form(sv):
     agree to rounding: far tighter than the oracle tolerance."""
     cfg = small_config("c0", R=4, k=0, H=64, kv_lens=(1100, 64, 1, 700), shuffled=True, vocab=64)
     inp = make_inputs(cfg, seed=14)
-    with stacked(sv, True):
-        o1, l1 = _attention(sv, inp, 1)
-    with stacked(sv, False):
-        o2, l2 = _attention(sv, inp, 1)
+    o1, l1 = _attention(sv, inp, 1, form=sv.FORM_STACKED)
+    o2, l2 = _attention(sv, inp, 1, form=sv.FORM_TWO_CTA)
     assert torch.equal(l1, l2)
     a, b = o1.double(), o2.double()
     rel = float(torch.linalg.norm(a - b) / torch.linalg.norm(b))
@@ -155,11 +143,9 @@ def test_auto_splits_count_one_cta_per_unit(sv):
     """The automatic split count of the stacked form fills the SMs with one
     CTA per (request, split)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    with stacked(sv, sv.STACKED_AUTO):
-        s_auto = sv.num_splits_for(64, 1, 64, 24)
-        s_short = sv.num_splits_for(2, 4, 8, 2)  # 1-2 tile units keep the two-CTA form
-    with stacked(sv, False):
-        s_off = sv.num_splits_for(64, 1, 64, 24)
+    s_auto = sv.num_splits_for(64, 1, 64, 24, sv.FORM_AUTO)
+    s_short = sv.num_splits_for(2, 4, 8, 2, sv.FORM_AUTO)  # 1-2 tile units keep the two-CTA form
+    s_off = sv.num_splits_for(64, 1, 64, 24, sv.FORM_TWO_CTA)
     assert s_auto == max(1, min(sms // 64, 12))
     assert s_off == max(1, min(sms // 128, 12))
     assert s_short == 1

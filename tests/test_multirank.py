@@ -54,9 +54,13 @@ def test_two_rank_max_over_ranks():
     assert res[0][5] != res[1][5]                             # independent replica inputs
 
 
-def test_single_rank_is_plain_mean():
+def test_single_rank_statistics():
     import sys
     sys.path.insert(0, ROOT)
     import bench
-    assert bench.max_over_ranks([1.0, 3.0], "cpu", 1) == pytest.approx(2.0)
+    xs = [5.0, 1.0, 2.0, 3.0, 4.0, 100.0]
+    assert bench.max_over_ranks(xs, "cpu", 1) == pytest.approx(3.5)  # median: one outlier moves it not
+    assert bench.max_over_ranks(xs, "cpu", 1, "mean") == pytest.approx(115.0 / 6)
+    st = bench.step_stats(list(range(1, 12)))
+    assert (st["p10"], st["median"], st["p90"]) == (2, 6, 10)
     assert bench.replica_throughput(2.0, 1) == pytest.approx(500.0)
