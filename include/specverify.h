@@ -62,6 +62,9 @@ typedef enum {
 #define SV_DEV_BAD_PAGE  0x1  /* block_table entry < 0 or >= num_pages was needed */
 #define SV_DEV_BAD_BOUND 0x2  /* kv_bounds[t] < 0 or > max_pages_per_req*page_size */
 #define SV_DEV_TIMEOUT   0x4  /* a bounded in-kernel wait gave up                 */
+/* only in the index-checking debug build (compiled with -DSPECVERIFY_DEBUG):
+ * an index or address check failed and its access was skipped */
+#define SV_DEV_DEBUG_CHECK 0x8
 
 #define SV_LATENT_DIM 512
 #define SV_PAGE_SIZE 64

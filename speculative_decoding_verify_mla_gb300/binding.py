@@ -58,12 +58,14 @@ class SpecVerifyError(RuntimeError):
 
 
 def load_library(path: str | None = None) -> ctypes.CDLL:
-    """Load (once) the compiled library; raises if it has not been built."""
+    """Load (once) the compiled library; raises if it has not been built.
+    The environment variable SPECVERIFY_LIBRARY names another build of it
+    (e.g. the index-checking debug build) to load instead."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = path or LIB_PATH
+        path = path or os.environ.get("SPECVERIFY_LIBRARY") or LIB_PATH
         if not os.path.exists(path):
             raise RuntimeError(
                 f"{path} is missing: build it first "

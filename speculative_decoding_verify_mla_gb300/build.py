@@ -1,9 +1,13 @@
 """Build libspecverify.so (all CUDA sources, sm_103a) in-tree.
 
-    python -m speculative_decoding_verify_mla_gb300.build
+    python -m speculative_decoding_verify_mla_gb300.build [--debug]
 
 The translation units compile in parallel, then link into one shared library
-next to this file.  The CUDA runtime is linked as a shared library so that it
+next to this file.  --debug builds libspecverify_debug.so instead: the same
+sources compiled with -DSPECVERIFY_DEBUG, whose kernels check their shared-
+memory, TMEM and global indexes before every access (a failed check sets
+SV_DEV_DEBUG_CHECK in the status word, prints its line and skips the access);
+load it by pointing SPECVERIFY_LIBRARY at it.  The CUDA runtime is linked as a shared library so that it
 is the same runtime instance torch uses (streams and the current device are
 shared).  No GPU is needed to build.
 """
@@ -21,6 +25,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libspecverify.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
+DEBUG_BUILD_DIR = os.path.join(PKG_DIR, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libspecverify_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
@@ -54,24 +60,27 @@ def _deps() -> list[str]:
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    flags = NVCC_FLAGS + (["-DSPECVERIFY_DEBUG"] if debug else [])
+    if not force and up_to_date(lib_path):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -86,7 +95,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
     libdir = _cuda_lib_dir(nvcc)
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath," + libdir]
     if verbose:
@@ -94,9 +103,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     res = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if res.returncode != 0:
         raise RuntimeError("link failed:\n" + res.stdout.decode(errors="replace"))
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

@@ -111,6 +111,9 @@ __global__ void __launch_bounds__(kCombineThreads)
   // (every split's partial is written, as zeros when its range is empty, so
   // they can be read before the weights are known).
   using P = Partial<kBf16>;
+  // debug build (no status word here: a failure is reported by its line)
+  SV_DCHECK(S >= 1 && S <= SV_MAX_SPLITS && rin >= 0 && rin < slot_rows && slot0 >= 0 && row < rows &&
+                col0 + 128 + 4 <= 512, nullptr);
   float l0 = -INFINITY, l1 = -INFINITY;
   if (lane < S) l0 = ld_dep_f32(part_lse + (slot0 + lane) * slot_rows + rin);
   if (lane + 32 < S) l1 = ld_dep_f32(part_lse + (slot0 + lane + 32) * slot_rows + rin);

@@ -179,6 +179,7 @@ struct VerifyParams {
   int gate_dim;             // 512: elementwise gate [T][H][512]; 1: head-wise gate [T][H]
   float kv_scale;           // fp8 KV: the pool's scale (1 for bf16 KV)
   const uint8_t* kv8;       // fp8 KV: the e4m3 page pool [pages][64][512]
+  long long part_lse_entries;  // part_lse elements the workspace holds (0 with one split)
 };
 
 // Two e4m3 codes (low byte first) -> two f16 (low half first); exact.
@@ -189,6 +190,7 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
 }
 
 __device__ __forceinline__ int load_bound(const VerifyParams& p, int tok) {
+  if (!SV_DCHECK(tok >= 0 && tok < p.R * p.q_per_req, p.status)) return 0;
   int b = __ldg(p.kv_bounds + tok);
   const int cap = p.max_pages * kTileN;
   if (b < 0 || b > cap) {
@@ -256,6 +258,12 @@ __device__ __forceinline__ void store_boxes(const EpilogueCtx& c, int bx0, int b
   const bool gate_ok = elem_gate && warp_wait(c.gate_full, 0, c.abort_flag, c.p->status);
   const uint8_t* const gs = c.sptr + c.off_q;
   const uint32_t st0 = c.sbase + c.off_own;
+#ifdef SPECVERIFY_DEBUG
+  constexpr uint32_t kMapBytes = (uint32_t)KernelShape<false, false>::kSmemUsed;
+  auto smem_in = [&](uint32_t a, uint32_t bytes) { return a >= c.sbase && a + bytes <= c.sbase + kMapBytes; };
+#endif
+  SV_DCHECK(bx0 >= 0 && bx1 <= 4 && (c.tmem & 0xFFFFu) + kTmemCols <= 512u && wq * 32 + 32 <= 128, c.p->status);
+  SV_DCHECK(!row_gate || !valid || row_g < c.p->rows_total, c.p->status);
 #pragma unroll 1
   for (int bx = bx0; bx < bx1; ++bx) {
     uint32_t va[32], vb[32];  // columns 64 bx .. +31 and 64 bx + 32 .. +63
@@ -274,7 +282,8 @@ __device__ __forceinline__ void store_boxes(const EpilogueCtx& c, int bx0, int b
       const uint32_t off = (uint32_t)bx * kQBoxBytes + row_off + (((uint32_t)u ^ swz) << 4);
       uint32_t ow[4];
       if (elem_gate) {
-        const uint4 graw = gate_ok ? *reinterpret_cast<const uint4*>(gs + off) : make_uint4(0u, 0u, 0u, 0u);
+        const bool g_in = SV_DCHECK(smem_in(c.sbase + c.off_q + off, 16), c.p->status);
+        const uint4 graw = gate_ok && g_in ? *reinterpret_cast<const uint4*>(gs + off) : make_uint4(0u, 0u, 0u, 0u);
         const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -288,11 +297,12 @@ __device__ __forceinline__ void store_boxes(const EpilogueCtx& c, int bx0, int b
         for (int e = 0; e < 4; ++e)
           ow[e] = pack_bf16x2(v(8 * u + 2 * e) * fs, v(8 * u + 2 * e + 1) * fs);
       }
-      *reinterpret_cast<uint4*>(stage + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      if (SV_DCHECK(smem_in(st0 + off, 16), c.p->status))
+        *reinterpret_cast<uint4*>(stage + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
     }
     fence_proxy_async_smem();
     named_bar_sync(bar_id, 128);
-    if (leader) {
+    if (leader && SV_DCHECK(smem_in(st0 + bx * kQBoxBytes, kQBoxBytes), c.p->status)) {
       if constexpr (!kStack) {
         if (c.fused)
           tma_store_3d(c.tmap_out, st0 + bx * kQBoxBytes, c.half * kDHalf + bx * 64, c.m_tile * kMTile, c.r);
@@ -355,6 +365,13 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
   const uint32_t q_own_free = bar0 + 8u * 21;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sptr + kOffBar + 8 * kNumBars);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(sptr + kOffBar + 8 * kNumBars + 4);
+#ifdef SPECVERIFY_DEBUG
+  // debug build: this CTA's shared-memory map is [sbase, sbase + kSmemUsed)
+  auto smem_in = [&](uint32_t a, uint32_t bytes) {
+    return a >= sbase && a + bytes <= sbase + (uint32_t)K::kSmemUsed;
+  };
+  SV_DCHECK(sbase + (uint32_t)K::kSmemUsed <= raw + (uint32_t)K::kSmemBytes, p.status);
+#endif
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -366,6 +383,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     // balanced plan: wait for the plan kernel, then read this CTA's unit
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if ((int)blockIdx.x >= ld_dep_s32(p.plan_header + 1)) return;  // spare CTA
+    SV_DCHECK((long long)blockIdx.x < (long long)gridDim.x, p.status);
     const int4 u = ld_dep_i4(p.units + blockIdx.x);
     r = u.x;
     m_tile = u.y >> 1;
@@ -385,6 +403,10 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     fused = (S == 1);
   }
   const int Mq = p.H * p.q_per_req;
+  SV_DCHECK(r >= 0 && r < p.R && m_tile >= 0 && m_tile < p.n_mtiles && (half == 0 || half == 1), p.status);
+  SV_DCHECK(!p.units || (plan_lo <= plan_hi && plan_hi <= p.max_pages), p.status);
+  SV_DCHECK(fused || (long long)(p.units ? slot : s_idx) * p.part_w_stride + (long long)(p.units ? 0 : r) * Mq +
+                             Mq <= p.part_lse_entries, p.status);
 
   // warp 0: start the dependent loads of the set-up (bounds -> block table ->
   // KV tiles) from L2 rather than HBM: prefetch the request's bound and
@@ -432,11 +454,13 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       mbar_arrive_expect_tx(q_own_full, kQHalfBytes);
 #pragma unroll
       for (int b = 0; b < 4; ++b)
-        tma_load_3d(oth0 + b * kQBoxBytes, &tmap_q, q_own_full, half * kDHalf + b * 64, m_tile * kMTile, r);
+        if (SV_DCHECK(smem_in(oth0 + b * kQBoxBytes, kQBoxBytes), p.status))
+          tma_load_3d(oth0 + b * kQBoxBytes, &tmap_q, q_own_full, half * kDHalf + b * 64, m_tile * kMTile, r);
       mbar_arrive_expect_tx(q_tma, kQHalfBytes);
 #pragma unroll
       for (int b = 0; b < 4; ++b)
-        tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_tma, (1 - half) * kDHalf + b * 64, m_tile * kMTile, r);
+        if (SV_DCHECK(smem_in(q_s + b * kQBoxBytes, kQBoxBytes), p.status))
+          tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_tma, (1 - half) * kDHalf + b * 64, m_tile * kMTile, r);
     } else {
       // stacked: tmap_q has 64-row boxes.  Latent 0..255 of the (at most 64)
       // query rows into rows 0..63 of the staging boxes; latent 256..511
@@ -444,10 +468,13 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       // score rows L and L + 64 are the same query row.
       mbar_arrive_expect_tx(q_own_full, kQHalfBytes / 2);
 #pragma unroll
-      for (int b = 0; b < 4; ++b) tma_load_3d(oth0 + b * kQBoxBytes, &tmap_q, q_own_full, b * 64, 0, r);
+      for (int b = 0; b < 4; ++b)
+        if (SV_DCHECK(smem_in(oth0 + b * kQBoxBytes, kQBoxBytes / 2), p.status))
+          tma_load_3d(oth0 + b * kQBoxBytes, &tmap_q, q_own_full, b * 64, 0, r);
       mbar_arrive_expect_tx(q_tma, kQHalfBytes);
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
+        if (!SV_DCHECK(smem_in(q_s + b * kQBoxBytes, kQBoxBytes), p.status)) continue;
         tma_load_3d(q_s + b * kQBoxBytes, &tmap_q, q_tma, kDHalf + b * 64, 0, r);
         tma_load_3d(q_s + b * kQBoxBytes + kQBoxBytes / 2, &tmap_q, q_tma, kDHalf + b * 64, 0, r);
       }
@@ -461,6 +488,14 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+#ifdef SPECVERIFY_DEBUG
+  // debug build: TMEM address a (lane << 16 | column) with `cols` columns
+  // from it, and the 32 lanes from its lane, inside this CTA's allocation
+  auto tmem_in = [&](uint32_t a, uint32_t cols) {
+    const uint32_t c0 = tmem & 0xFFFFu, c = a & 0xFFFFu, ln = a >> 16;
+    return c >= c0 && c + cols <= c0 + kTmemCols && ln + 32 <= 128 && (ln & 31) == 0;
+  };
+#endif
 
   // ---- unit geometry (every thread derives the same values)
   const int t_first = (m_tile * kMTile) / p.H;
@@ -471,6 +506,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
   {
     const int cap = p.max_pages * kTileN;
     bool bad = false;
+    SV_DCHECK((long long)(r + 1) * p.q_per_req <= (long long)p.R * p.q_per_req, p.status);
     for (int t = 0; t < p.q_per_req; ++t) {
       const int b = __ldg(p.kv_bounds + r * p.q_per_req + t);
       bad |= (b < 0) | (b > cap);
@@ -501,6 +537,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       for (int s = 0; s < kOthStages; ++s) last_oth[s] = -1;
       for (int it = 0; it < ntiles; ++it) {
         const int j = lo + it;
+        if (!SV_DCHECK(j >= 0 && j < p.max_pages, p.status)) break;
         int page = __ldg(p.block_table + (long long)r * p.max_pages + j);
         if (page < 0 || page >= p.num_pages) {
           if (p.status) atomicOr(p.status, SV_DEV_BAD_PAGE);
@@ -513,8 +550,10 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         mbar_arrive_expect_tx(own_full(so), kHalfTileBytes);
 #pragma unroll
         for (int b = 0; b < 4; ++b)
-          tma_load_2d(own0 + so * kHalfTileBytes + b * kBoxBytes, &tmap_kv, own_full(so),
-                      half * kDHalf + b * 64, page * kTileN);
+          if (SV_DCHECK(smem_in(own0 + so * kHalfTileBytes + b * kBoxBytes, kBoxBytes) && page < p.num_pages,
+                        p.status))
+            tma_load_2d(own0 + so * kHalfTileBytes + b * kBoxBytes, &tmap_kv, own_full(so),
+                        half * kDHalf + b * 64, page * kTileN);
         last_own[so] = ro;
         // other half: scores only (its ring holds the staged query half until
         // the softmax warps have moved it into TMEM)
@@ -525,8 +564,10 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         mbar_arrive_expect_tx(oth_full(sx), kHalfTileBytes);
 #pragma unroll
         for (int b = 0; b < 4; ++b)
-          tma_load_2d(oth0 + sx * kHalfTileBytes + b * kBoxBytes, &tmap_kv, oth_full(sx),
-                      (1 - half) * kDHalf + b * 64, page * kTileN);
+          if (SV_DCHECK(smem_in(oth0 + sx * kHalfTileBytes + b * kBoxBytes, kBoxBytes) && page < p.num_pages,
+                        p.status))
+            tma_load_2d(oth0 + sx * kHalfTileBytes + b * kBoxBytes, &tmap_kv, oth_full(sx),
+                        (1 - half) * kDHalf + b * 64, page * kTileN);
         last_oth[sx] = rx;
       }
       // every copy this CTA started has landed before teardown
@@ -590,6 +631,8 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         break;
       }
       const int rows_valid = maxb_tile - (lo + it) * kTileN;
+      SV_DCHECK(rows_valid > 0 && smem_in(own0 + so * kHalfTileBytes, kHalfTileBytes) &&
+                    smem_in(oth0 + sx * kHalfTileBytes, kHalfTileBytes), p.status);
       if (rows_valid < kTileN) {
         // the own half is V of P V; the other half feeds only scores (its
         // slack columns are masked by selection), except in the stacked form
@@ -606,17 +649,22 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         const uint32_t k_hi = (uint32_t)(ko_desc >> 32);  // the same for every K-major operand
         const uint32_t q_lo = (uint32_t)q_desc;
         const uint32_t d = tmem + kTmemS + 64u * sb;
+        const bool dbg_ok = SV_DCHECK(tmem_in(d, 64) && tmem_in(tmem + kTmemQ, 128) && smem_in(q_s, kQHalfBytes) &&
+                                          smem_in(own0 + so * kHalfTileBytes, kHalfTileBytes) &&
+                                          smem_in(oth0 + sx * kHalfTileBytes, kHalfTileBytes), p.status);
         // B = K tile, K-major, 128-byte swizzle: step 16 latent columns (32
         // bytes) inside a box, next box every 4 steps.
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          mma_ts_w(d, tmem + kTmemQ + 8u * kk, ko_lo + (uint32_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4),
-                   k_hi, idesc_s, kk > 0 ? 1u : 0u);
+          if (dbg_ok)
+            mma_ts_w(d, tmem + kTmemQ + 8u * kk, ko_lo + (uint32_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4),
+                     k_hi, idesc_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          mma_ss_w(d, q_lo + (uint32_t)(((kk >> 2) * kQBoxBytes + (kk & 3) * 32) >> 4), k_hi,
-                   kx_lo + (uint32_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4), k_hi, idesc_s, 1u);
+          if (dbg_ok)
+            mma_ss_w(d, q_lo + (uint32_t)(((kk >> 2) * kQBoxBytes + (kk & 3) * 32) >> 4), k_hi,
+                     kx_lo + (uint32_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4), k_hi, idesc_s, 1u);
         }
         mma_commit(s_full(sb));
         if constexpr (!kStack) mma_commit(oth_empty(sx));  // stacked: P V reads it too
@@ -645,6 +693,10 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       tc_fence_after();
       if (lane == 0) {
         const uint32_t a = tmem + kTmemS + 64u * sb;
+        const bool dbg_ok = SV_DCHECK(tmem_in(a, 64) && tmem_in(tmem + kTmemO, 256) &&
+                                          smem_in(own0 + so * kHalfTileBytes, kHalfTileBytes) &&
+                                          (!kStack || smem_in(oth0 + sx * kHalfTileBytes, kHalfTileBytes)),
+                                      p.status);
         // descriptors differ only in the 14-bit start-address field, which
         // never carries (shared addresses < 256 KB): one add per MMA
         const uint64_t pv_desc0 = sdesc_sw128(own0 + so * kHalfTileBytes, kBoxBytes, 1024);
@@ -658,16 +710,18 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
           const uint32_t px_lo = (uint32_t)sdesc_sw128(oth0 + sx * kHalfTileBytes, kBoxBytes, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts_w(tmem + kTmemO, a + 32u + 8u * kk, px_lo + (uint32_t)((kk * 16 * 128) >> 4), pv_hi, idesc_pv,
-                     (i > 0 || kk > 0) ? 1u : 0u);
+            if (dbg_ok)
+              mma_ts_w(tmem + kTmemO, a + 32u + 8u * kk, px_lo + (uint32_t)((kk * 16 * 128) >> 4), pv_hi, idesc_pv,
+                       (i > 0 || kk > 0) ? 1u : 0u);
           mma_commit(oth_empty(sx));
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           // B = V tile (own half), MN-major: N = 256 latent columns in four
           // 64-wide boxes (LBO = box stride), K = 16 KV rows per step (SBO = 8-row stride).
-          mma_ts_w(tmem + kTmemO, a + 8u * kk, pv_lo + (uint32_t)((kk * 16 * 128) >> 4), pv_hi, idesc_pv,
-                   (kStack || i > 0 || kk > 0) ? 1u : 0u);
+          if (dbg_ok)
+            mma_ts_w(tmem + kTmemO, a + 8u * kk, pv_lo + (uint32_t)((kk * 16 * 128) >> 4), pv_hi, idesc_pv,
+                     (kStack || i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(own_empty(so));
         mma_commit(pv_done(sb));
@@ -699,6 +753,8 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       // c * 16 KB + 128 i, 16-byte chunks swizzled by i mod 8) -> TMEM (bf16
       // pairs per 32-bit column); rows past M arrived as zeros
       const uint8_t* const qrow = sptr + kOffOth + qi * 128;
+      SV_DCHECK(smem_in(oth0 + qi * 128, 3 * kQBoxBytes + 128) && tmem_in(tmem + lane_off + kTmemQ, 128) &&
+                    (lane_off >> 16) == (uint32_t)(wq * 32), p.status);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
@@ -728,12 +784,14 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       if constexpr (!kStack) {
 #pragma unroll
         for (int b = 0; b < 4; ++b)
-          tma_load_3d(q_s + b * kQBoxBytes, &tmap_gate, gate_full, half * kDHalf + b * 64,
-                      m_tile * kMTile, r);
+          if (SV_DCHECK(smem_in(q_s + b * kQBoxBytes, kQBoxBytes), p.status))
+            tma_load_3d(q_s + b * kQBoxBytes, &tmap_gate, gate_full, half * kDHalf + b * 64,
+                        m_tile * kMTile, r);
       } else {
         // rows 64h .. 64h+63 of box b: latent 256h + 64b .. +63 (64-row boxes)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
+          if (!SV_DCHECK(smem_in(q_s + b * kQBoxBytes, kQBoxBytes), p.status)) continue;
           tma_load_3d(q_s + b * kQBoxBytes, &tmap_gate, gate_full, b * 64, 0, r);
           tma_load_3d(q_s + b * kQBoxBytes + kQBoxBytes / 2, &tmap_gate, gate_full, kDHalf + b * 64, 0, r);
         }
@@ -754,6 +812,8 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       if (!warp_wait(s_full(sb), par, abort_flag, p.status)) { ok = false; break; }
       if (fused && p.gate_dim != 1 && it == ntiles - 1 && leader)
         load_gate();  // last score GEMM is done
+      SV_DCHECK(tmem_in(tmem + lane_off + kTmemS + 64u * sb, 64) && tmem_in(tmem + lane_off + kTmemO, 256),
+                p.status);
       tc_fence_after();
       float x[64];
       {
@@ -859,10 +919,12 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     const bool row_gate = fused && p.gate_dim == 1;
     const bool elem_gate = fused && p.gate_dim != 1;
     float g_row = 1.f;
+    SV_DCHECK(!row_gate || !valid || row_g < p.rows_total, p.status);
     if (row_gate) g_row = valid ? fast_sigmoid(__bfloat162float(p.gate[row_g])) : 0.f;
     const bool gate_ok = elem_gate && warp_wait(gate_full, 0, abort_flag, p.status);
     const uint8_t* const gs = sptr + kOffQ;
     const uint32_t st0 = sbase + kOffOwn;
+    SV_DCHECK(tmem_in(tmem + lane_off + kTmemO, 256), p.status);
 #pragma unroll 1
     for (int bx = 0; bx < 4; ++bx) {
       uint32_t va[32], vb[32];  // columns 64 bx .. +31 and 64 bx + 32 .. +63
@@ -881,7 +943,9 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         const uint32_t off = (uint32_t)bx * kQBoxBytes + row_off + (((uint32_t)u ^ swz) << 4);
         uint32_t ow[4];
         if (elem_gate) {
-          const uint4 graw = gate_ok ? *reinterpret_cast<const uint4*>(gs + off) : make_uint4(0u, 0u, 0u, 0u);
+          const bool g_in = SV_DCHECK(smem_in(q_s + off, 16), p.status);
+          const uint4 graw =
+              gate_ok && g_in ? *reinterpret_cast<const uint4*>(gs + off) : make_uint4(0u, 0u, 0u, 0u);
           const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -895,11 +959,12 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
           for (int e = 0; e < 4; ++e)
             ow[e] = pack_bf16x2(v(8 * u + 2 * e) * f, v(8 * u + 2 * e + 1) * f);
         }
-        *reinterpret_cast<uint4*>(stage + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        if (SV_DCHECK(smem_in(st0 + off, 16), p.status))
+          *reinterpret_cast<uint4*>(stage + off) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
       }
       fence_proxy_async_smem();
       named_bar_sync(kEpilogueBarId, 128);
-      if (leader) {
+      if (leader && SV_DCHECK(smem_in(st0 + bx * kQBoxBytes, kQBoxBytes), p.status)) {
         if constexpr (!kStack) {
           if (fused)
             tma_store_3d(&tmap_out, st0 + bx * kQBoxBytes, half * kDHalf + bx * 64, m_tile * kMTile, r);
@@ -923,11 +988,12 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     }
     if (valid && (kStack ? i < 64 : half == 0)) {
       if (fused) {
-        p.lse[row_g] = lse_v;
+        if (SV_DCHECK(row_g >= 0 && row_g < p.rows_total, p.status)) p.lse[row_g] = lse_v;
       } else {
         const long long w = p.units ? slot : s_idx;
         const long long z = p.units ? 0 : r;
-        p.part_lse[w * p.part_w_stride + z * Mq + f] = lse_v;
+        const long long e = w * p.part_w_stride + z * Mq + f;
+        if (SV_DCHECK(e >= 0 && e < p.part_lse_entries, p.status)) p.part_lse[e] = lse_v;
       }
     }
     if (leader) tma_store_wait_read();  // SMEM stays valid until the stores have read it
@@ -947,6 +1013,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       const int32_t* bt_row = p.block_table + (long long)r * p.max_pages + lo;
       uint4 buf[16];
       auto load_tile = [&](int it) {
+        SV_DCHECK(lo + it >= 0 && lo + it < p.max_pages, p.status);
         int page = __ldg(bt_row + it);
         if (page < 0 || page >= p.num_pages) {
           if (ct == 0 && p.status) atomicOr(p.status, SV_DEV_BAD_PAGE);
@@ -964,6 +1031,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         ok = mbar_wait<false>(q_tma, 0, abort_flag, p.status);
         if (ok) {
           uint4* const qs = reinterpret_cast<uint4*>(sptr + kOffQ);
+          SV_DCHECK(smem_in(q_s, kQHalfBytes), p.status);
 #pragma unroll 4
           for (int u = 0; u < kQHalfBytes / 16 / 128; ++u) {
             const uint4 w = qs[u * 128 + ct];
@@ -1004,8 +1072,10 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
           w1.z = e4m3x2_to_f16x2(v.w);
           w1.w = e4m3x2_to_f16x2(v.w >> 16);
           uint8_t* const rb = ring + b * kBoxBytes + row * 128;
-          *reinterpret_cast<uint4*>(rb + (((uint32_t)j0 ^ (uint32_t)(row & 7)) << 4)) = w0;
-          *reinterpret_cast<uint4*>(rb + (((uint32_t)(j0 + 1) ^ (uint32_t)(row & 7)) << 4)) = w1;
+          if (SV_DCHECK(smem_in(smem_u32(rb), 128) && row < kTileN, p.status)) {
+            *reinterpret_cast<uint4*>(rb + (((uint32_t)j0 ^ (uint32_t)(row & 7)) << 4)) = w0;
+            *reinterpret_cast<uint4*>(rb + (((uint32_t)(j0 + 1) ^ (uint32_t)(row & 7)) << 4)) = w1;
+          }
         }
         fence_proxy_async_smem();  // the tensor cores read what the threads wrote
         mbar_arrive(own_full(so));
@@ -1190,7 +1260,8 @@ __global__ void __launch_bounds__(kPlanThreads)
       const int pos = atomicAdd(&s_cnt[bk], 2 * n_mt);
       const int sl = sr >= 2 ? base[r] + j : -1;
       for (int u = 0; u < 2 * n_mt; ++u)
-        units[pos + u] = make_int4(r, u, plo | (phi << 16), sl);
+        if (SV_DCHECK(pos + u >= 0 && pos + u < units_max && sl < slots_max, status))
+          units[pos + u] = make_int4(r, u, plo | (phi << 16), sl);
     }
   }
   __syncthreads();
@@ -1465,6 +1536,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   prm.gate_dim = gate_dim;
   prm.kv_scale = kv_fp8 ? kv_scale : 1.0f;
   prm.kv8 = kv_fp8 ? static_cast<const uint8_t*>(kv_pages) : nullptr;
+  prm.part_lse_entries = balanced ? (long long)PL.slots_max * Mq_ll : (S > 1 ? (long long)S * T * H : 0);
   // fp8: the pool scale multiplies every score (folded into the scale here)
   // and the output (applied in the epilogue)
   if (kv_fp8) prm.scale_log2 *= kv_scale;

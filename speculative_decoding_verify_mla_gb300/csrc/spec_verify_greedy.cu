@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "specverify.h"
+#include "sv_ptx.cuh"
 
 namespace sv {
 namespace {
@@ -77,6 +78,8 @@ __global__ void __launch_bounds__(kGreedyThreads)
   const long long lo = (long long)c * chunk;
   const long long hi = min((long long)V, lo + chunk);
   const float* row = logits + (long long)t * V;
+  // debug build (no status word here: a failure is reported by its line)
+  SV_DCHECK(t >= 0 && t < T && lo >= 0 && lo <= hi && hi <= V, nullptr);
 
   // ---- chunk scan: each thread walks its elements in increasing index order
   float best_v = -INFINITY;
@@ -140,6 +143,7 @@ __global__ void __launch_bounds__(kGreedyThreads)
   __threadfence();
   for (int tt = tid; tt < T; tt += kGreedyThreads) {
     const int rq = tt / (k + 1), j = tt - rq * (k + 1);
+    SV_DCHECK(rq < R && (j == k || (long long)rq * k + j < (long long)R * k), nullptr);
     const int d = (j < k) ? __ldg(draft_tokens + (long long)rq * k + j) : 0;
     const unsigned long long key = __ldcg(row_key + tt);
     const int a = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));

@@ -4,11 +4,35 @@
 #pragma once
 
 #include <cstdint>
+#include <cstdio>
 #include <cuda_runtime.h>
 
 #include "specverify.h"
 
 namespace sv {
+
+// ---------------------------------------------------------------- index-checking debug build
+// Compiled with -DSPECVERIFY_DEBUG, the kernels check the shared-memory, TMEM
+// and global indexes of their accesses (and the addresses behind every TMA
+// copy and MMA operand) before making them.  A failed check ORs
+// SV_DEV_DEBUG_CHECK into the caller's status word, prints the source line
+// (at most a few lines per translation unit) and the access is skipped; the
+// kernel goes on (a skipped copy or MMA can then make a bounded wait give up,
+// which also reports through the status word).  In the normal build every
+// check is the constant `true` and compiles away.
+#ifdef SPECVERIFY_DEBUG
+static __device__ int g_debug_prints;
+static __device__ __noinline__ bool debug_fail(int32_t* status, int line) {
+  if (status) atomicOr(status, SV_DEV_DEBUG_CHECK);
+  if (atomicAdd(&g_debug_prints, 1) < 16)
+    printf("specverify debug check failed: %s line %d, block %d thread %d\n", __FILE__, line,
+           (int)blockIdx.x, (int)threadIdx.x);
+  return false;
+}
+#define SV_DCHECK(cond, status) ((cond) ? true : ::sv::debug_fail((status), __LINE__))
+#else
+#define SV_DCHECK(cond, status) true
+#endif
 
 // Every in-kernel wait gives up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
