@@ -828,13 +828,21 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         }
       }
       const int lim = b_i - (lo + it) * kTileN;  // columns >= lim are masked
-      float tmax = -INFINITY;
+      if (__any_sync(0xFFFFFFFFu, lim < kTileN)) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float v = (c < lim) ? x[c] * p.scale_log2 : -INFINITY;
-        x[c] = v;
-        tmax = fmaxf(tmax, v);
+        for (int c = 0; c < 64; ++c) x[c] = (c < lim) ? x[c] : -INFINITY;
       }
+      // row max of the raw scores in eight independent chains (a single
+      // fmaxf chain over 64 columns is a long serial dependency); the scale
+      // is positive, so the scaled maximum is the maximum times the scale
+      float mx[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mx[c] = fmaxf(x[c], x[c + 8]);
+#pragma unroll
+      for (int c = 16; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) mx[c] = fmaxf(mx[c], mx[c + 4]);
+      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
       // lazy rescale: move the reference max only when it grows by > 2^8
       const bool move = tmax > m_ref + kRescaleThreshold;
       const float m_new = move ? tmax : m_ref;
@@ -862,15 +870,17 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       m_ref = m_new;
       const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
       uint32_t pk[32];
-      float psum = 0.f;
+      // p = 2^(scale x - m) with one fma feeding the exp2 (a masked x is
+      // -inf and gives 0); the row sum in eight independent chains
+      float ps[8];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = fast_exp2(x[2 * c] - msub);
-        const float p1 = fast_exp2(x[2 * c + 1] - msub);
-        psum += p0 + p1;
+        const float p0 = fast_exp2(fmaf(x[2 * c], p.scale_log2, -msub));
+        const float p1 = fast_exp2(fmaf(x[2 * c + 1], p.scale_log2, -msub));
+        ps[c & 7] = (c < 8) ? p0 + p1 : ps[c & 7] + (p0 + p1);
         pk[c] = kF8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
       }
-      l_sum += psum;
+      l_sum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       if constexpr (!kStack) {
         tmem_st32(tmem + lane_off + kTmemS + 64u * sb, pk);  // P over the consumed scores
       } else {

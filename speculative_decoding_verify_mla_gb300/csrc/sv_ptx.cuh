@@ -31,7 +31,8 @@ static __device__ __noinline__ bool debug_fail(int32_t* status, int line) {
 }
 #define SV_DCHECK(cond, status) ((cond) ? true : ::sv::debug_fail((status), __LINE__))
 #else
-#define SV_DCHECK(cond, status) true
+__host__ __device__ __forceinline__ constexpr bool dcheck_pass() { return true; }
+#define SV_DCHECK(cond, status) ::sv::dcheck_pass()
 #endif
 
 // Every in-kernel wait gives up after this many nanoseconds of %globaltimer.
