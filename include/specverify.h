@@ -389,8 +389,8 @@ sv_status spec_verify_sampled(const float* logits, int R, int k, int V, float te
  *    SV_ERR_WORKSPACE before anything is enqueued.
  *  - The first call on a device looks up the array's address with that device
  *    current; make that first call before any stream capture begins.
- *  - Each call clears the part of the array it uses (counters, per-row keys,
- *    per-request slots: 256 + 12 T bytes) with cudaMemsetAsync on `stream`
+ *  - Each call clears the part of the array it uses (the counter and the
+ *    per-row keys: 256 + 8 T bytes) with cudaMemsetAsync on `stream`
  *    before its kernel; nothing is allocated or freed.
  *  - All calls share the one array: calls whose kernels may overlap on the
  *    GPU (unordered streams, several host threads) race and give wrong

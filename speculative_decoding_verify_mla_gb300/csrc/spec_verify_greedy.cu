@@ -8,16 +8,16 @@
 //
 // One launch.  The [T][V] fp32 logits are cut into chunks of C floats (about
 // four CTAs per SM); each CTA streams one chunk with coalesced 128-bit loads
-// (eight in flight per thread), reduces it to a 64-bit key (order-preserving
-// value bits << 32 | ~index, so the max key is the max value at the lowest
-// index) and folds it into its row's key with a 64-bit atomicMax.  (Many
-// smaller CTAs stream a little faster but pay the per-CTA atomic, fence and
-// ticket latency once per wave: slower overall on GB300.)  The CTA that takes
-// the last ticket reads the row keys and the drafts in one round trip, marks
-// every mismatching draft with an atomicMax of (k - j) on its request's slot
-// (a zero slot means every draft matched), then writes accepted / next token /
-// trimmed kv_lens, and leaves the ticket and all slots zero again.  Nothing
-// waits on another CTA.
+// (about eight in flight per thread: the load of the next round's slot is
+// issued as soon as a value is taken), reduces it to a 64-bit key
+// (order-preserving value bits << 32 | ~index, so the max key is the max
+// value at the lowest index) and folds it into its row's key with a 64-bit
+// atomicMax.  (Many smaller CTAs stream a little faster but pay the per-CTA
+// atomic, fence and ticket latency once per wave: slower overall on GB300.)
+// The CTA that takes the last ticket gives each thread whole requests: it
+// reads the request's row keys and drafts in one round trip, decodes the
+// argmax ids and writes accepted / next token / trimmed kv_lens, and leaves
+// the ticket and every row key zero again.  Nothing waits on another CTA.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kGreedyThreads)
                          const int32_t* __restrict__ kv_lens_in, int32_t* __restrict__ argmax_ids,
                          int32_t* __restrict__ accepted, int32_t* __restrict__ next_tokens,
                          int32_t* __restrict__ kv_lens_out, unsigned int* __restrict__ ticket,
-                         unsigned long long* row_key, int* mis) {
+                         unsigned long long* row_key) {
   // Shared memory stays under 1 KB so that this kernel can share an SM with
   // the attention kernel (which leaves ~1.8 KB of the SM's shared memory).
   __shared__ unsigned long long s_warp[kGreedyThreads / 32];
@@ -88,19 +88,32 @@ __global__ void __launch_bounds__(kGreedyThreads)
     const float4* p4 = reinterpret_cast<const float4*>(row + lo);
     const int n4 = (int)((hi - lo) >> 2);
     int i = tid;
-    // eight independent 16-byte loads per thread in flight per round
-    for (; i + 7 * kGreedyThreads < n4; i += 8 * kGreedyThreads) {
+    // rounds of eight 16-byte loads per thread, pipelined: as soon as a
+    // value is taken, the load of the same slot of the next round is
+    // issued, so about eight loads stay in flight per thread without a
+    // second buffer (elements are still reduced in increasing index order,
+    // which keeps the lowest index on ties)
+    constexpr int kRound = 8 * kGreedyThreads;
+    if (i + 7 * kGreedyThreads < n4) {
       float4 a[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) a[u] = ld_stream_f4(p4 + i + u * kGreedyThreads);
+      while (true) {
+        const int j = i + kRound;
+        const bool more = j + 7 * kGreedyThreads < n4;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint32_t base = (uint32_t)(lo + 4ll * (i + u * kGreedyThreads));
-        if (best_i == 0xFFFFFFFFu) { best_v = a[u].x; best_i = base; }
-        else if (a[u].x > best_v) { best_v = a[u].x; best_i = base; }
-        if (a[u].y > best_v) { best_v = a[u].y; best_i = base + 1; }
-        if (a[u].z > best_v) { best_v = a[u].z; best_i = base + 2; }
-        if (a[u].w > best_v) { best_v = a[u].w; best_i = base + 3; }
+        for (int u = 0; u < 8; ++u) {
+          const float4 v = a[u];
+          if (more) a[u] = ld_stream_f4(p4 + j + u * kGreedyThreads);
+          const uint32_t base = (uint32_t)(lo + 4ll * (i + u * kGreedyThreads));
+          if (best_i == 0xFFFFFFFFu) { best_v = v.x; best_i = base; }
+          else if (v.x > best_v) { best_v = v.x; best_i = base; }
+          if (v.y > best_v) { best_v = v.y; best_i = base + 1; }
+          if (v.z > best_v) { best_v = v.z; best_i = base + 2; }
+          if (v.w > best_v) { best_v = v.w; best_i = base + 3; }
+        }
+        i = j;
+        if (!more) break;
       }
     }
     for (; i < n4; i += kGreedyThreads) {
@@ -134,29 +147,43 @@ __global__ void __launch_bounds__(kGreedyThreads)
   __syncthreads();
   if (!s_last) return;
 
-  // ---- last CTA: the row keys and the drafts in one round trip; a draft j
-  // that differs from its target's argmax raises its request's slot to k - j
-  // (the largest value marks the first mismatch); then accepted, next token
-  // and trim from the slots.  Every slot is left zero for the next call.
-  // Global writes and atomics of this block are visible to all its threads
-  // after __syncthreads; the reads go to L2 (.cg).
+  // ---- last CTA: one thread per request reads its tokens' row keys and its
+  // drafts in one round trip (all loads issued before any is used, eight
+  // tokens at a time), decodes the argmax ids, and finds the first token j
+  // whose draft differs from a_j (or j = k): accepted = j, next token = a_j,
+  // kv_lens_out = kv_lens_in - (k - j).  Every row key and the ticket are
+  // left zero for the next call.  The keys were raised with atomics by the
+  // other CTAs before their ticket; the reads go to L2 (.cg).
   __threadfence();
-  for (int tt = tid; tt < T; tt += kGreedyThreads) {
-    const int rq = tt / (k + 1), j = tt - rq * (k + 1);
-    SV_DCHECK(rq < R && (j == k || (long long)rq * k + j < (long long)R * k), nullptr);
-    const int d = (j < k) ? __ldg(draft_tokens + (long long)rq * k + j) : 0;
-    const unsigned long long key = __ldcg(row_key + tt);
-    const int a = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-    argmax_ids[tt] = a;
-    row_key[tt] = 0ull;
-    if (j < k && d != a) atomicMax(mis + rq, k - j);
-  }
-  __syncthreads();
   for (int r = tid; r < R; r += kGreedyThreads) {
-    const int n = k - __ldcg(mis + r);
-    mis[r] = 0;
+    const int t0 = r * (k + 1);
+    int n = -1, nxt = 0;
+    for (int j0 = 0; j0 <= k; j0 += 8) {
+      unsigned long long key[8];
+      int d[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;
+        SV_DCHECK(j > k || (long long)t0 + j < (long long)T, nullptr);
+        key[u] = (j <= k) ? __ldcg(row_key + t0 + j) : 0ull;
+        d[u] = (j < k) ? __ldg(draft_tokens + (long long)r * k + j) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;
+        if (j <= k) {
+          const int a = (int)(0xFFFFFFFFu - (uint32_t)(key[u] & 0xFFFFFFFFull));
+          argmax_ids[t0 + j] = a;
+          row_key[t0 + j] = 0ull;
+          if (n < 0 && (j == k || d[u] != a)) {
+            n = j;
+            nxt = a;
+          }
+        }
+      }
+    }
     accepted[r] = n;
-    next_tokens[r] = __ldcg(argmax_ids + r * (k + 1) + n);
+    next_tokens[r] = nxt;
     kv_lens_out[r] = kv_lens_in[r] - (k - n);
   }
   if (tid == 0) *ticket = 0u;  // leave the workspace zeroed for the next call
@@ -175,11 +202,10 @@ int greedy_chunk(int T, int V) {
 }  // namespace
 }  // namespace sv
 
-// Workspace: ticket header, then the row keys [T] and the per-request
-// mismatch slots [T >= R]; all zero at rest.
+// Workspace: ticket header, then the row keys [T]; all zero at rest.
 extern "C" size_t sv_greedy_workspace_bytes(int T, int V) {
   if (T <= 0 || V <= 0) return sv::kGreedyHeader;
-  return sv::kGreedyHeader + (size_t)T * sizeof(unsigned long long) + (size_t)T * sizeof(int);
+  return sv::kGreedyHeader + (size_t)T * sizeof(unsigned long long);
 }
 
 namespace sv {
@@ -221,10 +247,9 @@ sv_status greedy_launch(const float* logits, int T, int V, int R, int k, const i
   const bool vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
   auto* ticket = reinterpret_cast<unsigned int*>(workspace);
   auto* row_key = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + kGreedyHeader);
-  auto* mis = reinterpret_cast<int*>(row_key + T);
   greedy_verify_kernel<<<(unsigned)blocks, kGreedyThreads, 0, stream>>>(
       logits, T, V, R, k, chunk, nchunks, vec4, draft_tokens, kv_lens_in, argmax_ids, accepted,
-      next_tokens, kv_lens_out, ticket, row_key, mis);
+      next_tokens, kv_lens_out, ticket, row_key);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_LAUNCH;
 }
 
@@ -255,9 +280,8 @@ extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R
 // a serving engine that has already handed (nearly) all of HBM to its own
 // KV-cache pool and forbids further cudaMalloc calls, or a plugin hosted by a
 // framework that owns the device allocator.  Such a caller cannot provide the
-// greedy workspace.  This entry point keeps that scratch (the ticket counter,
-// the per-row argmax keys and the per-request mismatch slots) in a fixed
-// file-scope device array instead.
+// greedy workspace.  This entry point keeps that scratch (the ticket counter
+// and the per-row argmax keys) in a fixed file-scope device array instead.
 //
 // Limits and sharing:
 //  * The array holds kNoAllocScratchBytes (512 KiB) on every GPU that loads
@@ -276,9 +300,9 @@ extern "C" sv_status spec_verify_greedy(const float* logits, int T, int V, int R
 //    cudaDeviceReset of the device may keep the context handle while the
 //    array moves, so this entry point must not be used on a device after the
 //    process has reset it.
-//  * The counter, keys and slots must start at zero: each call clears the
-//    part it uses with a cudaMemsetAsync on the same stream before the kernel
-//    runs (every call also leaves them zero).
+//  * The counter and keys must start at zero: each call clears the part it
+//    uses with a cudaMemsetAsync on the same stream before the kernel runs
+//    (every call also leaves them zero).
 // No cudaMalloc, cudaFree or other allocating routine is called.
 namespace sv {
 namespace {

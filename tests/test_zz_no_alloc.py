@@ -93,14 +93,14 @@ def test_noalloc_large_small_large():
 
 @pytest.mark.gpu
 def test_noalloc_largest_batch_that_fits():
-    """The largest T whose scratch (256 + 12 T bytes) fits in 512 KiB, with
+    """The largest T whose scratch (256 + 8 T bytes) fits in 512 KiB, with
     planted maxima and ties, against the workspace entry point."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import speculative_decoding_verify_mla_gb300 as sv
     lib = _lib()
     k = 1
-    T = (SCRATCH_BYTES - 256) // 12
+    T = (SCRATCH_BYTES - 256) // 8
     T -= T % (k + 1)
     R, V = T // (k + 1), 12
     assert sv.greedy_workspace_bytes(T, V) <= SCRATCH_BYTES < sv.greedy_workspace_bytes(T + 2, V)
@@ -120,7 +120,7 @@ def test_noalloc_rejects_bad_calls_without_device_pointers():
         pytest.skip("no CUDA device")
     lib = _lib()
     f = lib.spec_verify_greedy_noalloc
-    T, V = 1 << 16, 1 << 20  # 12 bytes of scratch per token: more than 512 KiB
+    T, V = 1 << 16, 1 << 20  # 8 bytes of scratch per token: more than 512 KiB
     assert f(None, T, V, T, 0, None, None, None, None, None, None, None) == 1   # SV_ERR_NULL
     assert f(None, 7, V, 2, 3, None, None, None, None, None, None, None) == 2   # T != R (k + 1)
     assert f(None, 0, V, 0, 3, None, None, None, None, None, None, None) == 0   # nothing to do
