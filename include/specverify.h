@@ -71,6 +71,8 @@ typedef enum {
 #define SV_MAX_SPLITS 64
 /* num_splits value selecting the balanced split plan (see mla_verify_decode). */
 #define SV_SPLITS_BALANCED (-1)
+/* num_splits value selecting the wave split mode (see mla_verify_decode). */
+#define SV_SPLITS_WAVE (-2)
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* sv_status_string(sv_status s);
@@ -123,6 +125,15 @@ const char* sv_status_string(sv_status s);
  *                   (n_tiles = 128-row tiles per request), so that requests of
  *                   very different lengths give the SMs equal work; the
  *                   pieces run longest first.  One extra small kernel.
+ *                 SV_SPLITS_WAVE (-2): for batches whose 2 * n_tiles * R
+ *                   CTAs fill the SMs more than once but less than twice:
+ *                   requests 0..k-1 are not split and fill the first wave,
+ *                   each other request is cut into s uniform pieces that
+ *                   fill the second, with k = floor(SMs / (2 n_tiles)) and
+ *                   s = max(2, floor(SMs / (2 n_tiles (R - k)))) (at most
+ *                   max_pages_per_req / 2); SV_ERR_SHAPE where that does not
+ *                   apply.  The merge kernel then reads only the split
+ *                   requests' rows.
  *                 0: automatic (sv_mla_verify_num_splits).
  *                 The result does not depend on the choice beyond rounding.
  *   workspace     device scratch of at least
@@ -166,9 +177,11 @@ const char* sv_status_string(sv_status s);
  * form (it only looks at the sizes, never at device data):
  * SV_SPLITS_BALANCED when R >= 2, max_pages_per_req >= 64 and
  * 2 * ceil(H*q_per_req/128) * R <= SMs (long contexts whose units fit the SMs
- * once), else a uniform count that fills the SMs once with >= 2 KV tiles per
- * split, counting one CTA per (request, row tile, split) when the stacked
- * form will be taken for it and two otherwise.  The same count serves the
+ * once); SV_SPLITS_WAVE when those CTAs fill the SMs more than once but less
+ * than twice (and the stacked form is not taken); else a uniform count that
+ * fills the SMs once with >= 2 KV tiles per split, counting one CTA per
+ * (request, row tile, split) when the stacked form will be taken for it and
+ * two otherwise.  The same count serves the
  * fp8 entry point.  sv_mla_verify_workspace_bytes accepts any num_splits
  * value mla_verify_decode accepts except 0 (resolve it first). */
 int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pages_per_req, int form);

@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     FORM_STACKED,
     FORM_TWO_CTA,
     SV_SPLITS_BALANCED,
+    SV_SPLITS_WAVE,
     SpecVerifyError,
     attention_workspace_bytes,
     greedy_workspace,

@@ -25,6 +25,7 @@ SV_LATENT_DIM = 512
 SV_PAGE_SIZE = 64
 SV_MAX_SPLITS = 64
 SV_SPLITS_BALANCED = -1
+SV_SPLITS_WAVE = -2
 # kernel form of the attention call (SV_FORM_*), chosen per call
 FORM_AUTO, FORM_TWO_CTA, FORM_STACKED = 0, 1, 2
 SV_DEV_BAD_PAGE = 0x1

@@ -65,6 +65,8 @@ __device__ __forceinline__ void fma4(float4& acc, float w, float4 v) {
 // `row` of a [S][rows] table.  Balanced plan (plan_splits != NULL): request r
 // = row / Mq owns slots plan_base[r] .. + plan_splits[r] - 1 of a [slots][Mq]
 // table, and a request with one piece was finished by the attention kernel.
+// Wave mode (wave_k >= 0): request r >= wave_k owns slots (r - wave_k) S ..
+// + S - 1 of a [slots][Mq] table; the grid covers rows row_begin.. only.
 // kFirst: splits whose partials are loaded with the weights (chosen from S at
 // launch, so that few splits keep few registers and many warps resident).
 template <bool kBf16, int kFirst>
@@ -73,12 +75,13 @@ __global__ void __launch_bounds__(kCombineThreads)
                        const float* __restrict__ part_lse,
                        int S_uniform, long long rows, const __nv_bfloat16* __restrict__ gate,
                        __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out,
-                       const int* plan_splits, const int* plan_base, int Mq, int gate_dim) {
+                       const int* plan_splits, const int* plan_base, int Mq, int gate_dim,
+                       long long row_begin, int wave_k) {
   // one warp per half row (256 columns): lane owns columns 128j + 4 lane .. +3, j = 0, 1
   const int lane = threadIdx.x & 31;
   const long long hrow = (long long)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
-  if (hrow >= 2 * rows) return;
-  const long long row = hrow >> 1;
+  if (hrow >= 2 * (rows - row_begin)) return;
+  const long long row = row_begin + (hrow >> 1);
   const int col0 = (int)(hrow & 1) * 256 + 4 * lane;
   // the gate does not depend on the attention kernel: fetch it first
   // (elementwise [T][H][512], or one value per row when head-wise)
@@ -102,6 +105,11 @@ __global__ void __launch_bounds__(kCombineThreads)
     S = ld_dep_s32(plan_splits + rq);
     if (S < 2) return;  // finished by the attention kernel
     slot0 = ld_dep_s32(plan_base + rq);
+    slot_rows = Mq;
+    rin = row - rq * Mq;
+  } else if (wave_k >= 0) {
+    const long long rq = row / Mq;
+    slot0 = (rq - wave_k) * S;
     slot_rows = Mq;
     rin = row - rq * Mq;
   }
@@ -189,9 +197,9 @@ __global__ void __launch_bounds__(kCombineThreads)
 cudaError_t launch_lse_combine(const void* part_o, bool bf16_partials, const float* part_lse, int S,
                                long long rows, const void* gate, void* out, float* lse,
                                cudaStream_t stream, const int* plan_splits, const int* plan_base,
-                               int Mq, int gate_dim) {
-  if (rows == 0) return cudaSuccess;
-  const long long blocks = (2 * rows + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
+                               int Mq, int gate_dim, long long row_begin, int wave_k) {
+  if (rows - row_begin <= 0) return cudaSuccess;
+  const long long blocks = (2 * (rows - row_begin) + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
   // programmatic dependent launch: the grid may start while the previous
   // kernel on the stream finishes; griddepcontrol.wait guards the partials
   cudaLaunchConfig_t cfg = {};
@@ -214,7 +222,7 @@ cudaError_t launch_lse_combine(const void* part_o, bool bf16_partials, const flo
   const int s_max = plan_splits ? 4 : S;
   auto launch = [&](auto kernel, const auto* po) {
     return cudaLaunchKernelEx(&cfg, kernel, po, part_lse, S, rows, g, o, lse, plan_splits, plan_base,
-                              Mq, gate_dim);
+                              Mq, gate_dim, row_begin, wave_k);
   };
   cudaError_t e;
   if (bf16_partials) {
@@ -249,7 +257,7 @@ extern "C" sv_status mla_lse_combine(const float* part_o, const float* part_lse,
     return SV_ERR_ALIGN;
   return sv::launch_lse_combine(part_o, false, part_lse, S, rows, gate, out, lse,
                                 reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr,
-                                1, SV_LATENT_DIM) == cudaSuccess
+                                1, SV_LATENT_DIM, 0, -1) == cudaSuccess
              ? SV_OK
              : SV_ERR_LAUNCH;
 }

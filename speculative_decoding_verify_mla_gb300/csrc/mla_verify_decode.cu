@@ -87,7 +87,7 @@ namespace sv {
 cudaError_t launch_lse_combine(const void* part_o, bool bf16_partials, const float* part_lse, int S,
                                long long rows, const void* gate, void* out, float* lse,
                                cudaStream_t stream, const int* plan_splits, const int* plan_base,
-                               int Mq, int gate_dim);
+                               int Mq, int gate_dim, long long row_begin = 0, int wave_k = -1);
 
 namespace {
 
@@ -180,6 +180,9 @@ struct VerifyParams {
   float kv_scale;           // fp8 KV: the pool's scale (1 for bf16 KV)
   const uint8_t* kv8;       // fp8 KV: the e4m3 page pool [pages][64][512]
   long long part_lse_entries;  // part_lse elements the workspace holds (0 with one split)
+  // wave split mode (wave_s > 0): requests 0..wave_k-1 whole, the others in
+  // wave_s uniform pieces whose partials go to slot (r - wave_k) wave_s + j
+  int wave_k, wave_s;
 };
 
 // Two e4m3 codes (low byte first) -> two f16 (low half first); exact.
@@ -308,7 +311,7 @@ __device__ __forceinline__ void store_boxes(const EpilogueCtx& c, int bx0, int b
           tma_store_3d(c.tmap_out, st0 + bx * kQBoxBytes, c.half * kDHalf + bx * 64, c.m_tile * kMTile, c.r);
         else
           tma_store_4d(c.tmap_part, st0 + bx * kQBoxBytes, c.half * kDHalf + bx * 64, c.m_tile * kMTile,
-                       c.p->units ? 0 : c.r, c.p->units ? c.slot : c.s_idx);
+                       (c.p->units || c.p->wave_s > 0) ? 0 : c.r, (c.p->units || c.p->wave_s > 0) ? c.slot : c.s_idx);
       } else {
         // staged rows 64h .. 64h+63 are latent 256h + 64bx .. +63 (64-row boxes)
 #pragma unroll
@@ -392,6 +395,25 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     plan_hi = (int)((unsigned)u.z >> 16);
     slot = u.w;
     fused = slot < 0;
+  } else if (p.wave_s > 0) {
+    // wave split mode: the whole requests' units first (they fill the first
+    // wave of CTAs), then the pieces of the others
+    half = (int)(blockIdx.x & 1);
+    const int unit = (int)(blockIdx.x >> 1);
+    const int whole = p.wave_k * p.n_mtiles;
+    if (unit < whole) {
+      r = unit / p.n_mtiles;
+      m_tile = unit % p.n_mtiles;
+      fused = true;
+    } else {
+      const int q = unit - whole;
+      const int rj = q / p.n_mtiles;
+      m_tile = q % p.n_mtiles;
+      r = p.wave_k + rj / p.wave_s;
+      s_idx = rj % p.wave_s;
+      slot = rj;
+      fused = false;
+    }
   } else {
     // latent half of O owned by this CTA (stacked: both, in the two lane halves)
     half = kStack ? 0 : (int)(blockIdx.x & 1);
@@ -402,10 +424,13 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     r = rm / p.n_mtiles;
     fused = (S == 1);
   }
+  // partials addressed by slot ([slot][Mq] rows: balanced plan, wave mode) or
+  // by (split, request) ([S][R][Mq] rows: uniform splits)
+  const bool slotted = p.units != nullptr || p.wave_s > 0;
   const int Mq = p.H * p.q_per_req;
   SV_DCHECK(r >= 0 && r < p.R && m_tile >= 0 && m_tile < p.n_mtiles && (half == 0 || half == 1), p.status);
   SV_DCHECK(!p.units || (plan_lo <= plan_hi && plan_hi <= p.max_pages), p.status);
-  SV_DCHECK(fused || (long long)(p.units ? slot : s_idx) * p.part_w_stride + (long long)(p.units ? 0 : r) * Mq +
+  SV_DCHECK(fused || (long long)(slotted ? slot : s_idx) * p.part_w_stride + (long long)(slotted ? 0 : r) * Mq +
                              Mq <= p.part_lse_entries, p.status);
 
   // warp 0: start the dependent loads of the set-up (bounds -> block table ->
@@ -519,8 +544,9 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
   int lo = plan_lo, hi = plan_hi;
   if (!p.units) {
     const int n_r = (maxb_req + kTileN - 1) / kTileN;
-    lo = (int)((long long)s_idx * n_r / S);
-    hi = (int)((long long)(s_idx + 1) * n_r / S);
+    const int s_r = p.wave_s > 0 ? (fused ? 1 : p.wave_s) : S;  // this request's pieces
+    lo = (int)((long long)s_idx * n_r / s_r);
+    hi = (int)((long long)(s_idx + 1) * n_r / s_r);
   }
   const int hi_eff = min(hi, (maxb_tile + kTileN - 1) / kTileN);
   const int ntiles = max(0, hi_eff - lo);
@@ -980,7 +1006,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
             tma_store_3d(&tmap_out, st0 + bx * kQBoxBytes, half * kDHalf + bx * 64, m_tile * kMTile, r);
           else
             tma_store_4d(&tmap_part, st0 + bx * kQBoxBytes, half * kDHalf + bx * 64, m_tile * kMTile,
-                         p.units ? 0 : r, p.units ? slot : s_idx);
+                         slotted ? 0 : r, slotted ? slot : s_idx);
         } else {
           // staged rows 64h .. 64h+63 are latent 256h + 64bx .. +63 (64-row boxes)
 #pragma unroll
@@ -1000,8 +1026,8 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       if (fused) {
         if (SV_DCHECK(row_g >= 0 && row_g < p.rows_total, p.status)) p.lse[row_g] = lse_v;
       } else {
-        const long long w = p.units ? slot : s_idx;
-        const long long z = p.units ? 0 : r;
+        const long long w = slotted ? slot : s_idx;
+        const long long z = slotted ? 0 : r;
         const long long e = w * p.part_w_stride + z * Mq + f;
         if (SV_DCHECK(e >= 0 && e < p.part_lse_entries, p.status)) p.part_lse[e] = lse_v;
       }
@@ -1357,6 +1383,29 @@ int auto_splits(int R, int q_per_req, int H, int max_pages, int sm_count, int fo
   return fill_splits(2ll * R * n_mt, max_pages, sm_count);
 }
 
+// Wave split mode, for batches whose unsplit units (2 per row tile) fill the
+// SMs more than once but less than twice: the first k requests stay whole
+// and fill the first wave, the other R - k are cut into s uniform pieces that
+// fill the second wave, so no SM idles behind a second round of whole
+// requests while every unit still pays its fixed cost only once or twice.
+//   k = floor(SMs / (2 n_mt)),   s = max(2, floor(SMs / (2 n_mt (R - k)))),
+// each piece keeping at least 2 KV tiles.  False when the mode does not
+// apply (one wave or more than two, fewer than 4 tiles per request).
+inline bool wave_params(long long R, long long n_mt, long long max_pages, int sms, int* k, int* s) {
+  const long long units = 2 * n_mt * R;
+  if (units <= sms || units >= 2ll * sms || max_pages < 4) return false;
+  const long long kk = sms / (2 * n_mt);
+  if (kk < 1 || kk >= R) return false;
+  long long ss = sms / (2 * n_mt * (R - kk));
+  if (ss < 2) ss = 2;
+  if (ss > max_pages / 2) ss = max_pages / 2;
+  if (ss > SV_MAX_SPLITS) ss = SV_MAX_SPLITS;
+  if (ss < 2) return false;
+  *k = (int)kk;
+  *s = (int)ss;
+  return true;
+}
+
 inline bool misaligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0;
 }
@@ -1414,12 +1463,25 @@ extern "C" int sv_mla_verify_num_splits(int R, int q_per_req, int H, int max_pag
   const long long n_mt = ((long long)H * q_per_req + sv::kMTile - 1) / sv::kMTile;
   if (R >= 2 && max_pages_per_req >= 64 && max_pages_per_req <= 0xFFFF && 2 * n_mt * R <= sms)
     return SV_SPLITS_BALANCED;
+  // the wave mode for batches of two-CTA units between one and two waves
+  // of the SMs (the C = 32 verify batch: 72.4 -> 62.1 us on GB300; other
+  // (k, s) measured 62.1-66.2 us)
+  int wk = 0, ws = 0;
+  if (form != SV_FORM_STACKED && !(H * (long long)q_per_req <= 64 && form == SV_FORM_AUTO) &&
+      sv::wave_params(R, n_mt, max_pages_per_req, sms, &wk, &ws))
+    return SV_SPLITS_WAVE;
   return sv::auto_splits(R, q_per_req, H, max_pages_per_req, sms, form);
 }
 
 extern "C" size_t sv_mla_verify_workspace_bytes(int T, int H, int num_splits) {
   if (T <= 0 || H <= 0) return 0;
   if (num_splits == SV_SPLITS_BALANCED) return sv::plan_workspace_bound(T, H, sv::current_sm_count());
+  if (num_splits == SV_SPLITS_WAVE) {
+    // slots * Mq <= (R - k) s Mq <= max(SMs / (2 n_mt), 2 (R - k)) * 128 n_mt
+    //            <= 64 SMs + 2 T H rows (Mq <= 128 n_mt, (R - k) Mq <= T H)
+    const size_t slot_rows = (size_t)64 * sv::current_sm_count() + 2 * (size_t)T * (size_t)H;
+    return sv::align256(slot_rows * sv::kD * sizeof(__nv_bfloat16)) + slot_rows * sizeof(float);
+  }
   if (num_splits <= 1) return 0;
   const size_t rows = (size_t)T * (size_t)H;
   const size_t o_bytes = (size_t)num_splits * rows * sv::kD * sizeof(__nv_bfloat16);
@@ -1441,7 +1503,8 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   if (gate_dim != kD && gate_dim != 1) return SV_ERR_UNSUPPORTED;
   if (!valid_form(form)) return SV_ERR_UNSUPPORTED;
   if (page_size != SV_PAGE_SIZE) return SV_ERR_UNSUPPORTED;
-  if ((num_splits < 0 && num_splits != SV_SPLITS_BALANCED) || num_splits > SV_MAX_SPLITS)
+  if ((num_splits < 0 && num_splits != SV_SPLITS_BALANCED && num_splits != SV_SPLITS_WAVE) ||
+      num_splits > SV_MAX_SPLITS)
     return SV_ERR_SHAPE;
   if (num_splits == SV_SPLITS_BALANCED && max_pages_per_req > 0xFFFF) return SV_ERR_SHAPE;
   const long long T = (long long)R * q_per_req;
@@ -1462,8 +1525,12 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   const int S = num_splits != 0 ? num_splits
                                 : sv_mla_verify_num_splits(R, q_per_req, H, max_pages_per_req, form);
   const bool balanced = (S == SV_SPLITS_BALANCED);
+  const bool wave = (S == SV_SPLITS_WAVE);
   const long long Mq_ll = (long long)H * q_per_req;
   const int n_mt = (int)((Mq_ll + kMTile - 1) / kMTile);
+  int wave_k = 0, wave_s = 0;
+  if (wave && !wave_params(R, n_mt, max_pages_per_req, sm_count, &wave_k, &wave_s)) return SV_ERR_SHAPE;
+  const long long wave_slots = (long long)(R - wave_k) * wave_s;
   __nv_bfloat16* part_o = nullptr;
   float* part_lse = nullptr;
   PlanLayout PL{};
@@ -1478,6 +1545,13 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
     plan_base_ptr = static_cast<char*>(workspace);
     part_o = reinterpret_cast<__nv_bfloat16*>(plan_base_ptr + PL.part_o);
     part_lse = reinterpret_cast<float*>(plan_base_ptr + PL.part_lse);
+  } else if (wave) {
+    if (!workspace) return SV_ERR_WORKSPACE;
+    if (misaligned(workspace, 256)) return SV_ERR_ALIGN;
+    if (workspace_bytes < sv_mla_verify_workspace_bytes((int)T, H, SV_SPLITS_WAVE)) return SV_ERR_WORKSPACE;
+    part_o = static_cast<__nv_bfloat16*>(workspace);
+    part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        align256((size_t)wave_slots * Mq_ll * kD * sizeof(__nv_bfloat16)));
   } else if (S > 1) {
     if (!workspace) return SV_ERR_WORKSPACE;
     if (misaligned(workspace, 256)) return SV_ERR_ALIGN;
@@ -1489,7 +1563,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   const long long Mq = (long long)H * q_per_req;
   // stacked instance: requests of <= 64 query rows, uniform splits; its row
   // maps have 64-row boxes
-  const bool stack = !balanced && use_stack(Mq, max_pages_per_req, S, form);
+  const bool stack = !balanced && !wave && use_stack(Mq, max_pages_per_req, S, form);
   const int m_box = stack ? 64 : kMTile;
   CUtensorMap tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part;
   {
@@ -1506,8 +1580,9 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
                         : !encode_map(&tmap_gate, bf16, 2, q_latent, 3, row_dims, row_box)) ||
         !encode_map(&tmap_out, bf16, 2, out, 3, row_dims, row_box))
       return SV_ERR_ALIGN;
-    if (balanced) {
-      const cuuint64_t part_dims[4] = {(cuuint64_t)kD, (cuuint64_t)Mq, 1, (cuuint64_t)PL.slots_max};
+    if (balanced || wave) {
+      const cuuint64_t slots = balanced ? (cuuint64_t)PL.slots_max : (cuuint64_t)wave_slots;
+      const cuuint64_t part_dims[4] = {(cuuint64_t)kD, (cuuint64_t)Mq, 1, slots};
       const cuuint32_t part_box[4] = {64, (cuuint32_t)kMTile, 1, 1};
       if (!encode_map(&tmap_part, bf16, 2, part_o, 4, part_dims, part_box))
         return SV_ERR_ALIGN;
@@ -1546,13 +1621,20 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   prm.gate_dim = gate_dim;
   prm.kv_scale = kv_fp8 ? kv_scale : 1.0f;
   prm.kv8 = kv_fp8 ? static_cast<const uint8_t*>(kv_pages) : nullptr;
-  prm.part_lse_entries = balanced ? (long long)PL.slots_max * Mq_ll : (S > 1 ? (long long)S * T * H : 0);
+  prm.wave_k = 0;
+  prm.wave_s = 0;
+  prm.part_lse_entries = balanced ? (long long)PL.slots_max * Mq_ll
+                         : wave   ? wave_slots * Mq_ll
+                                  : (S > 1 ? (long long)S * T * H : 0);
+  prm.wave_k = wave_k;
+  prm.wave_s = wave_s;
   // fp8: the pool scale multiplies every score (folded into the scale here)
   // and the output (applied in the epilogue)
   if (kv_fp8) prm.scale_log2 *= kv_scale;
-  // long units (uniform splits of >= kTwoIssuerTiles tiles, or the balanced
-  // plan's pieces) take the instance with a second score issuer
-  const bool two = balanced || ((long long)max_pages_per_req + S - 1) / S >= kTwoIssuerTiles;
+  // long units (uniform splits of >= kTwoIssuerTiles tiles, the balanced
+  // plan's pieces, the wave mode's whole requests) take the instance with a
+  // second score issuer (a unit with fewer tiles runs on one issuer in it)
+  const bool two = balanced || wave || ((long long)max_pages_per_req + S - 1) / S >= kTwoIssuerTiles;
   auto kernel = kv_fp8 ? (stack ? (two ? mla_verify_kernel<true, true, true> : mla_verify_kernel<true, false, true>)
                                : (two ? mla_verify_kernel<true, true, false> : mla_verify_kernel<true, false, false>))
                        : (stack ? (two ? mla_verify_kernel<false, true, true> : mla_verify_kernel<false, false, true>)
@@ -1562,6 +1644,17 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   const int smem = KernelShape<false, false>::kSmemBytes;  // the same for every instance
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
+  if (wave) {
+    prm.part_w_stride = Mq_ll;
+    const long long ctas = 2ll * n_mt * (wave_k + wave_slots);
+    kernel<<<(unsigned)ctas, threads, smem, st>>>(tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part, prm);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_LAUNCH;
+    // merge only the rows of the split requests
+    if (launch_lse_combine(part_o, true, part_lse, wave_s, T * H, gate, out, lse, st, nullptr, nullptr,
+                           (int)Mq_ll, gate_dim, (long long)wave_k * Mq_ll, wave_k) != cudaSuccess)
+      return SV_ERR_LAUNCH;
+    return SV_OK;
+  }
   if (!balanced) {
     const long long ctas = (stack ? 1ll : 2ll) * R * prm.n_mtiles * S;
     if (ctas > 0x7FFFFFFFll) return SV_ERR_SHAPE;

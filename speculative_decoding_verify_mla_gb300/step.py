@@ -84,9 +84,12 @@ class VerifyStep:
     @property
     def attention_launches(self) -> int:
         """Kernels one mla_verify_decode call enqueues: the balanced plan adds a
-        plan kernel and the merge; uniform splits add the merge when S > 1."""
+        plan kernel and the merge; the wave mode and uniform splits (S > 1) add
+        the merge."""
         if self.num_splits == B.SV_SPLITS_BALANCED:
             return 3
+        if self.num_splits == B.SV_SPLITS_WAVE:
+            return 2
         return 1 + (1 if self.num_splits > 1 else 0)
 
     @property

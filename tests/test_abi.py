@@ -136,7 +136,7 @@ def test_sampled_host_checks(lib):
 
 
 def test_balanced_plan_host_checks(lib):
-    assert _attn_call(lib, splits=-2) == 2                       # only -1 is a valid negative
+    assert _attn_call(lib, splits=-3) == 2                       # only -1 and -2 are valid negatives
     assert _attn_call(lib, splits=-1) == 4                       # the plan needs a workspace
     assert _attn_call(lib, splits=-1, maxp=70000) == 2           # piece bounds are 16-bit
     from speculative_decoding_verify_mla_gb300 import SV_SPLITS_BALANCED, attention_workspace_bytes
@@ -145,10 +145,16 @@ def test_balanced_plan_host_checks(lib):
 
 
 def test_auto_split_choice(lib):
-    from speculative_decoding_verify_mla_gb300 import num_splits_for
+    from speculative_decoding_verify_mla_gb300 import SV_SPLITS_WAVE, attention_workspace_bytes, num_splits_for
     assert num_splits_for(1, 8, 64, 24) >= 1       # one request: uniform splits
     assert num_splits_for(16, 8, 64, 512) == -1    # long contexts, one wave: balanced plan
-    assert num_splits_for(32, 5, 64, 24) >= 1      # short contexts: uniform splits
+    # 32 requests x 3 row tiles x 2 halves = 192 CTAs: between one and two
+    # waves of the (fallback) 152 SMs -> the wave mode
+    assert num_splits_for(32, 5, 64, 24) == SV_SPLITS_WAVE == -2
+    assert num_splits_for(64, 1, 64, 24) >= 1      # 128 CTAs (stacked form): uniform splits
+    assert num_splits_for(20, 5, 64, 24) >= 1      # 120 CTAs fit one wave: uniform splits
+    assert num_splits_for(60, 5, 64, 24) >= 1      # 360 CTAs: more than two waves
+    assert attention_workspace_bytes(160, 64, -2) >= 7 * 3 * 320 * (1024 + 4)  # the split requests' slots
 
 
 def test_form_is_per_call(lib):

@@ -196,6 +196,38 @@ def test_attention_split_sweep(sv, splits):
     check_attention(out, lse, ref_o, ref_l, label=f"splits={splits}")
 
 
+def test_attention_wave_mode(sv):
+    """The wave split mode (the first k requests whole, the others in s
+    pieces) on 30 requests x 3 row tiles x 2 halves = 180 CTAs: ragged
+    contexts, zero bounds in whole and in split requests, NaN pool slack,
+    both gate shapes."""
+    rng = np.random.default_rng(21)
+    lens = tuple(int(x) for x in rng.integers(70, 700, size=30))
+    cfg = small_config("c2", R=30, k=4, H=64, kv_lens=lens, kv_len_range=None, shuffled=True, vocab=64)
+    inp = make_inputs(cfg, seed=21)
+    assert sv.num_splits_for(inp["R"], 5, 64, inp["max_pages"]) == sv.SV_SPLITS_WAVE
+    bounds = inp["kv_bounds"].copy()
+    bounds[[0, 3, 5 * 28 + 1, 5 * 29 + 4]] = 0  # whole requests 0 and 28's neighbours, split requests too
+    kv = inp["kv_bits"].copy()
+    for r in range(inp["R"]):
+        L = int(inp["kv_lens_in"][r])
+        kv[int(inp["block_table"][r, (L - 1) // 64]), L % 64 if L % 64 else 64:] = 0x7FC0
+    ref_o, ref_l = oracle_attention(inp, bounds=bounds, kv_bits=kv)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse = run_attention(sv, inp, num_splits=sv.SV_SPLITS_WAVE, kv_bits=kv, bounds=bounds, status=status)
+    assert int(status.item()) == 0
+    check_attention(out, lse, ref_o, ref_l, label="wave mode")
+    g_head = np.ascontiguousarray(inp["gate_bits"][:, :, 0])
+    ref_oh, ref_lh = oracle.ref_verify_attention(inp["q_bits"], kv, inp["block_table"], bounds, g_head, 5,
+                                                 inp["softmax_scale"])
+    d = device_inputs(inp, DEV)
+    out_h, lse_h = sv.mla_verify_decode(d["q"], bf16_tensor(kv, DEV), d["block_table"], i32(bounds, DEV),
+                                        bf16_tensor(g_head, DEV), 5, inp["softmax_scale"],
+                                        num_splits=sv.SV_SPLITS_WAVE)
+    torch.cuda.synchronize()
+    check_attention(out_h, lse_h, ref_oh, ref_lh, label="wave mode, head-wise gate")
+
+
 def test_attention_partials_layout(sv):
     """The split partials in the workspace follow the documented layout and
     equal the oracle's partials over the documented tile ranges."""
