@@ -63,11 +63,15 @@ class VerifyStep:
         (q_latent, gate, block_table, kv_bounds) is uploaded on the caller's
         stream ahead of the attention, ``ver`` (logits, draft_tokens,
         kv_lens_in) on the side stream ahead of the greedy verify, so the
-        logits copy overlaps the attention.  Returns the [3, R] results block
-        (accepted, next_tokens, kv_lens_out) on the caller's stream."""
+        logits copy overlaps the attention.  The logits copy starts only once
+        the attention inputs have landed: both copies share the host-to-device
+        bandwidth, and the attention waits for its inputs while the greedy
+        verify, much shorter, can wait for the logits.  Returns the [3, R]
+        results block (accepted, next_tokens, kv_lens_out) on the caller's
+        stream."""
         main = torch.cuda.current_stream(self.device)
-        self.side.wait_stream(main)
         att.upload()  # the small attention inputs first, so the attention can start
+        self.side.wait_stream(main)  # ... alone on the link
         with torch.cuda.stream(self.side):
             ver.upload()  # the logits copy overlaps the attention
         B.mla_verify_decode(att.dev["q_latent"], kv_pages, att.dev["block_table"], att.dev["kv_bounds"],
