@@ -75,9 +75,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <array>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include "sv_host.h"
 #include "sv_ptx.cuh"
@@ -180,6 +182,7 @@ struct VerifyParams {
   float kv_scale;           // fp8 KV: the pool's scale (1 for bf16 KV)
   const uint8_t* kv8;       // fp8 KV: the e4m3 page pool [pages][64][512]
   long long part_lse_entries;  // part_lse elements the workspace holds (0 with one split)
+  uint64_t wait_ns;             // short-wait instances: limit of every bounded wait (tests)
   // wave split mode (wave_s > 0): requests 0..wave_k-1 whole, the others in
   // wave_s uniform pieces whose partials go to slot (r - wave_k) wave_s + j
   int wave_k, wave_s;
@@ -205,8 +208,8 @@ __device__ __forceinline__ int load_bound(const VerifyParams& p, int tok) {
 
 // Bounded wait taken by a whole warp; all lanes get the same answer.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status) {
-  const bool ok = mbar_wait<false>(bar, parity, abort_flag, status);
+                                          int32_t* status, uint64_t limit_ns) {
+  const bool ok = mbar_wait<false>(bar, parity, abort_flag, status, limit_ns);
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
@@ -238,7 +241,7 @@ struct EpilogueCtx {
 // a named barrier over the 128 threads of the group and `leader` starts its
 // TMA tensor store (rows past M are dropped).  Used by the long-unit
 // instances, whose softmax warps and helper warps split the four boxes.
-template <bool kStack>
+template <bool kStack, bool kShortWaits>
 __device__ __forceinline__ void store_boxes(const EpilogueCtx& c, int bx0, int bx1, float scale, uint32_t bar_id,
                                             bool leader) {
   const int wq = c.warp & 3;
@@ -258,7 +261,8 @@ __device__ __forceinline__ void store_boxes(const EpilogueCtx& c, int bx0, int b
   const bool elem_gate = c.fused && c.p->gate_dim != 1;
   float g_row = 1.f;
   if (row_gate) g_row = valid ? fast_sigmoid(__bfloat162float(c.p->gate[row_g])) : 0.f;
-  const bool gate_ok = elem_gate && warp_wait(c.gate_full, 0, c.abort_flag, c.p->status);
+  const bool gate_ok = elem_gate && warp_wait(c.gate_full, 0, c.abort_flag, c.p->status,
+                                                      kShortWaits ? c.p->wait_ns : kWaitTimeoutNs);
   const uint8_t* const gs = c.sptr + c.off_q;
   const uint32_t st0 = c.sbase + c.off_own;
 #ifdef SPECVERIFY_DEBUG
@@ -331,7 +335,11 @@ __device__ __forceinline__ void store_boxes(const EpilogueCtx& c, int bx0, int b
 // Tensor maps: tmap_kv 2-D over the page pool [pages*64][512] bf16; tmap_q,
 // tmap_gate, tmap_out 3-D [R][M][512] bf16 (rows past a request's M fall out
 // of bounds: zero on load, dropped on store); tmap_part 4-D [S][R][M][512] fp32.
-template <bool kF8, bool kTwo, bool kStack>
+// kShortWaits: the test instances, whose bounded waits give up after
+// p.wait_ns instead of kWaitTimeoutNs (a compile-time limit costs the
+// production instances nothing in their wait loops; a limit read from the
+// parameters cost the long-context batch 2%).
+template <bool kF8, bool kTwo, bool kStack, bool kShortWaits>
 __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     mla_verify_kernel(const __grid_constant__ CUtensorMap tmap_kv,
                       const __grid_constant__ CUtensorMap tmap_q,
@@ -339,6 +347,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
                       const __grid_constant__ CUtensorMap tmap_out,
                       const __grid_constant__ CUtensorMap tmap_part, const VerifyParams p) {
   using K = KernelShape<kF8, kTwo>;
+  const uint64_t wait_ns = kShortWaits ? p.wait_ns : kWaitTimeoutNs;
   constexpr int kOwnStages = K::kOwnStages, kOthStages = K::kOthStages, kNumBars = K::kNumBars;
   constexpr int kOffQ = K::kOffQ, kOffOwn = K::kOffOwn, kOffOth = K::kOffOth, kOffBar = K::kOffBar;
   extern __shared__ uint8_t smem_raw[];
@@ -572,7 +581,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         // own half: scores and P V
         const int so = it % kOwnStages;
         const int ro = it / kOwnStages;
-        if (ro > 0 && !mbar_wait<false>(own_empty(so), (ro - 1) & 1, abort_flag, p.status)) break;
+        if (ro > 0 && !mbar_wait<false>(own_empty(so), (ro - 1) & 1, abort_flag, p.status, wait_ns)) break;
         mbar_arrive_expect_tx(own_full(so), kHalfTileBytes);
 #pragma unroll
         for (int b = 0; b < 4; ++b)
@@ -585,8 +594,8 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         // the softmax warps have moved it into TMEM)
         const int sx = it % kOthStages;
         const int rx = it / kOthStages;
-        if (it == 0 && !mbar_wait<false>(q_own_free, 0, abort_flag, p.status)) break;
-        if (rx > 0 && !mbar_wait<false>(oth_empty(sx), (rx - 1) & 1, abort_flag, p.status)) break;
+        if (it == 0 && !mbar_wait<false>(q_own_free, 0, abort_flag, p.status, wait_ns)) break;
+        if (rx > 0 && !mbar_wait<false>(oth_empty(sx), (rx - 1) & 1, abort_flag, p.status, wait_ns)) break;
         mbar_arrive_expect_tx(oth_full(sx), kHalfTileBytes);
 #pragma unroll
         for (int b = 0; b < 4; ++b)
@@ -628,8 +637,8 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     const int step = two ? 2 : 1;
     constexpr uint32_t idesc_s = kF8 ? idesc_f16_f32(128, 64, false, false) : idesc_bf16_f32(128, 64, false, false);
     const uint64_t q_desc = sdesc_sw128(q_s, 16, 1024);  // A of the other-half score MMAs
-    bool ok = ntiles > 0 && (warp == 1 || two) && warp_wait(q_ready, 0, abort_flag, p.status) &&
-              (kF8 || warp_wait(q_tma, 0, abort_flag, p.status));
+    bool ok = ntiles > 0 && (warp == 1 || two) && warp_wait(q_ready, 0, abort_flag, p.status, wait_ns) &&
+              (kF8 || warp_wait(q_tma, 0, abort_flag, p.status, wait_ns));
     bool issued = false;
     auto zero_tail = [&](uint8_t* tile, int rows_valid) {
       // rows no query row of this unit may see: zero them (pool slack may be
@@ -645,14 +654,14 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       const int so = it % kOwnStages;
       const int sx = it % kOthStages;
       const int sb = it & 1;
-      if (!warp_wait(own_full(so), (it / kOwnStages) & 1, abort_flag, p.status) ||
-          !warp_wait(oth_full(sx), (it / kOthStages) & 1, abort_flag, p.status)) {
+      if (!warp_wait(own_full(so), (it / kOwnStages) & 1, abort_flag, p.status, wait_ns) ||
+          !warp_wait(oth_full(sx), (it / kOthStages) & 1, abort_flag, p.status, wait_ns)) {
         ok = false;
         break;
       }
       // the score buffer is free once the P V of two tiles ago (which read
       // its P) has completed
-      if (it >= 2 && !warp_wait(pv_done(sb), ((it - 2) >> 1) & 1, abort_flag, p.status)) {
+      if (it >= 2 && !warp_wait(pv_done(sb), ((it - 2) >> 1) & 1, abort_flag, p.status, wait_ns)) {
         ok = false;
         break;
       }
@@ -715,7 +724,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       const int sb = i & 1;
       const int so = i % kOwnStages;
       const int sx = i % kOthStages;
-      if (!warp_wait(p_full(sb), (i >> 1) & 1, abort_flag, p.status)) break;
+      if (!warp_wait(p_full(sb), (i >> 1) & 1, abort_flag, p.status, wait_ns)) break;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t a = tmem + kTmemS + 64u * sb;
@@ -774,7 +783,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     const long long row_g = (long long)r * Mq + f;
     const int b_i = valid ? load_bound(p, r * p.q_per_req + t_loc) : 0;
 
-    if (ntiles > 0 && warp_wait(q_own_full, 0, abort_flag, p.status)) {
+    if (ntiles > 0 && warp_wait(q_own_full, 0, abort_flag, p.status, wait_ns)) {
       // this CTA's half of the query row, staged by TMA (row i of box c at
       // c * 16 KB + 128 i, 16-byte chunks swizzled by i mod 8) -> TMEM (bf16
       // pairs per 32-bit column); rows past M arrived as zeros
@@ -805,7 +814,9 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     }
     // Stage the gate tile (128 rows x 256 columns) into the Q region once no
     // score GEMM will read it again.
+    bool gate_loaded = false;  // the leader started the gate tile's copy
     auto load_gate = [&]() {
+      gate_loaded = true;
       mbar_arrive_expect_tx(gate_full, kQHalfBytes);
       if constexpr (!kStack) {
 #pragma unroll
@@ -826,7 +837,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     // an empty unit stages the gate at once, after the query copy into the
     // same region has landed
     if (fused && p.gate_dim != 1 && ntiles == 0 && leader &&
-        mbar_wait<false>(q_tma, 0, abort_flag, p.status))
+        mbar_wait<false>(q_tma, 0, abort_flag, p.status, wait_ns))
       load_gate();
 
     float m_ref = -INFINITY;  // running max (log2 units) used for exponentiation
@@ -835,7 +846,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     for (int it = 0; it < ntiles; ++it) {
       const int sb = it & 1;
       const uint32_t par = (it >> 1) & 1;
-      if (!warp_wait(s_full(sb), par, abort_flag, p.status)) { ok = false; break; }
+      if (!warp_wait(s_full(sb), par, abort_flag, p.status, wait_ns)) { ok = false; break; }
       if (fused && p.gate_dim != 1 && it == ntiles - 1 && leader)
         load_gate();  // last score GEMM is done
       SV_DCHECK(tmem_in(tmem + lane_off + kTmemS + 64u * sb, 64) && tmem_in(tmem + lane_off + kTmemO, 256),
@@ -876,7 +887,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       const float alpha = rescale_o ? exp2f(m_ref - m_new) : 1.0f;
       if (__any_sync(0xFFFFFFFFu, rescale_o)) {
         // O holds tiles < it: wait for PV(it-1), then scale the row in TMEM
-        if (!warp_wait(pv_done((it - 1) & 1), ((it - 1) >> 1) & 1, abort_flag, p.status)) {
+        if (!warp_wait(pv_done((it - 1) & 1), ((it - 1) >> 1) & 1, abort_flag, p.status, wait_ns)) {
           ok = false;
           break;
         }
@@ -929,7 +940,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     // helper warps the softmax warps do boxes 0..1 and hand 1/l over
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // a dependent merge may launch
     if (ok && ntiles > 0)
-      ok = warp_wait(pv_done((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
+      ok = warp_wait(pv_done((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, abort_flag, p.status, wait_ns);
     tc_fence_after();
     const bool have_o = ok && ntiles > 0;
     float inv_l = (l_sum > 0.f) ? 1.0f / l_sum : 0.f;
@@ -943,7 +954,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       named_bar_sync(kHandoffBarId, 256);
       const EpilogueCtx ctx{&p, &tmap_out, &tmap_part, sptr, sbase, tmem, gate_full, kOffOwn, kOffQ, abort_flag,
                             warp, lane, half, m_tile, r, s_idx, slot, Mq, fused};
-      store_boxes<kStack>(ctx, 0, 2, scale, kEpilogueBarId, leader);
+      store_boxes<kStack, kShortWaits>(ctx, 0, 2, scale, kEpilogueBarId, leader);
     } else {
     // the same box loop as store_boxes, all four boxes
     // staging: the KV rings are idle once the last P V has completed
@@ -957,7 +968,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
     float g_row = 1.f;
     SV_DCHECK(!row_gate || !valid || row_g < p.rows_total, p.status);
     if (row_gate) g_row = valid ? fast_sigmoid(__bfloat162float(p.gate[row_g])) : 0.f;
-    const bool gate_ok = elem_gate && warp_wait(gate_full, 0, abort_flag, p.status);
+    const bool gate_ok = elem_gate && warp_wait(gate_full, 0, abort_flag, p.status, wait_ns);
     const uint8_t* const gs = sptr + kOffQ;
     const uint32_t st0 = sbase + kOffOwn;
     SV_DCHECK(tmem_in(tmem + lane_off + kTmemO, 256), p.status);
@@ -1033,6 +1044,9 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       }
     }
     if (leader) tma_store_wait_read();  // SMEM stays valid until the stores have read it
+    // the gate tile's copy has landed before teardown, even when a wait gave
+    // up and the epilogue did not use it
+    if (leader && gate_loaded) drain_wait(gate_full, 0);
     __syncwarp();
   }
 
@@ -1064,7 +1078,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         load_tile(0);
         // the bf16 query half -> f16 in place (elementwise, so the swizzle
         // is kept); rows past M arrived as zeros
-        ok = mbar_wait<false>(q_tma, 0, abort_flag, p.status);
+        ok = mbar_wait<false>(q_tma, 0, abort_flag, p.status, wait_ns);
         if (ok) {
           uint4* const qs = reinterpret_cast<uint4*>(sptr + kOffQ);
           SV_DCHECK(smem_in(q_s, kQHalfBytes), p.status);
@@ -1079,13 +1093,13 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
         }
         // the other-half ring holds the staged query half until the softmax
         // warps have moved it into TMEM
-        if (ok) ok = mbar_wait<false>(q_own_free, 0, abort_flag, p.status);
+        if (ok) ok = mbar_wait<false>(q_own_free, 0, abort_flag, p.status, wait_ns);
       }
       for (int it = 0; ok && it < ntiles; ++it) {
         const int so = it % kOwnStages, ro = it / kOwnStages;
         const int sx = it % kOthStages, rx = it / kOthStages;
-        if (ro > 0) ok = mbar_wait<false>(own_empty(so), (ro - 1) & 1, abort_flag, p.status);
-        if (ok && rx > 0) ok = mbar_wait<false>(oth_empty(sx), (rx - 1) & 1, abort_flag, p.status);
+        if (ro > 0) ok = mbar_wait<false>(own_empty(so), (ro - 1) & 1, abort_flag, p.status, wait_ns);
+        if (ok && rx > 0) ok = mbar_wait<false>(oth_empty(sx), (rx - 1) & 1, abort_flag, p.status, wait_ns);
         if (!ok) break;
         uint8_t* const own_t = sptr + kOffOwn + so * kHalfTileBytes;
         uint8_t* const oth_t = sptr + kOffOth + sx * kHalfTileBytes;
@@ -1130,7 +1144,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
       const bool hl = (warp == K::kHelperLeaderWarp && lane == 0);
       const EpilogueCtx ctx{&p, &tmap_out, &tmap_part, sptr, sbase, tmem, gate_full, kOffOwn, kOffQ, abort_flag,
                             warp, lane, half, m_tile, r, s_idx, slot, Mq, fused};
-      store_boxes<kStack>(ctx, 2, 4, reinterpret_cast<const float*>(sptr + K::kOffRowScale)[(warp & 3) * 32 + lane],
+      store_boxes<kStack, kShortWaits>(ctx, 2, 4, reinterpret_cast<const float*>(sptr + K::kOffRowScale)[(warp & 3) * 32 + lane],
                           kHelperBarId, hl);
       if (hl) tma_store_wait_read();  // SMEM stays valid until the stores have read it
       __syncwarp();
@@ -1318,6 +1332,15 @@ int g_sm_count[kMaxDevices];
 bool g_attr_set[kMaxDevices];
 std::mutex g_dev_mu;
 
+// Every instance of the attention kernel: index kv_fp8 | two << 1 |
+// stack << 2 | short_waits << 3.
+using VerifyKernel = decltype(&mla_verify_kernel<false, false, false, false>);
+template <size_t... I>
+constexpr std::array<VerifyKernel, sizeof...(I)> verify_kernels(std::index_sequence<I...>) {
+  return {&mla_verify_kernel<(I & 1) != 0, (I & 2) != 0, (I & 4) != 0, (I & 8) != 0>...};
+}
+constexpr auto kVerifyKernels = verify_kernels(std::make_index_sequence<16>{});
+
 bool device_setup(int* sm_count) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
@@ -1327,15 +1350,8 @@ bool device_setup(int* sm_count) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
     constexpr int smem = KernelShape<false, false>::kSmemBytes;  // the same for every instance
     constexpr auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    if (cudaFuncSetAttribute(mla_verify_kernel<false, false, false>, attr, smem) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_verify_kernel<false, true, false>, attr, smem) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_verify_kernel<true, false, false>, attr, smem) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_verify_kernel<true, true, false>, attr, smem) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_verify_kernel<false, false, true>, attr, smem) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_verify_kernel<false, true, true>, attr, smem) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_verify_kernel<true, false, true>, attr, smem) != cudaSuccess ||
-        cudaFuncSetAttribute(mla_verify_kernel<true, true, true>, attr, smem) != cudaSuccess)
-      return false;
+    for (const VerifyKernel k : kVerifyKernels)
+      if (cudaFuncSetAttribute(k, attr, smem) != cudaSuccess) return false;
     g_sm_count[dev] = sms;
     g_attr_set[dev] = true;
   }
@@ -1497,7 +1513,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
                       int q_per_req, int max_pages_per_req, const int32_t* kv_bounds,
                       const void* gate, int gate_dim, int H, float softmax_scale, int num_splits,
                       int form, void* workspace, size_t workspace_bytes, void* out, float* lse,
-                      int32_t* status, sv_stream_t stream) {
+                      int32_t* status, sv_stream_t stream, uint64_t wait_ns = kWaitTimeoutNs) {
   if (R < 0 || q_per_req < 1 || H < 1 || max_pages_per_req < 0 || num_pages < 0)
     return SV_ERR_SHAPE;
   if (gate_dim != kD && gate_dim != 1) return SV_ERR_UNSUPPORTED;
@@ -1623,6 +1639,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   prm.kv8 = kv_fp8 ? static_cast<const uint8_t*>(kv_pages) : nullptr;
   prm.wave_k = 0;
   prm.wave_s = 0;
+  prm.wait_ns = wait_ns;
   prm.part_lse_entries = balanced ? (long long)PL.slots_max * Mq_ll
                          : wave   ? wave_slots * Mq_ll
                                   : (S > 1 ? (long long)S * T * H : 0);
@@ -1635,10 +1652,9 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   // plan's pieces, the wave mode's whole requests) take the instance with a
   // second score issuer (a unit with fewer tiles runs on one issuer in it)
   const bool two = balanced || wave || ((long long)max_pages_per_req + S - 1) / S >= kTwoIssuerTiles;
-  auto kernel = kv_fp8 ? (stack ? (two ? mla_verify_kernel<true, true, true> : mla_verify_kernel<true, false, true>)
-                               : (two ? mla_verify_kernel<true, true, false> : mla_verify_kernel<true, false, false>))
-                       : (stack ? (two ? mla_verify_kernel<false, true, true> : mla_verify_kernel<false, false, true>)
-                                : (two ? mla_verify_kernel<false, true, false> : mla_verify_kernel<false, false, false>));
+  const bool short_waits = wait_ns < kWaitTimeoutNs;
+  const VerifyKernel kernel =
+      kVerifyKernels[(kv_fp8 ? 1 : 0) | (two ? 2 : 0) | (stack ? 4 : 0) | (short_waits ? 8 : 0)];
   const int threads = kv_fp8 ? (two ? KernelShape<true, true>::kThreads : KernelShape<true, false>::kThreads)
                              : (two ? KernelShape<false, true>::kThreads : KernelShape<false, false>::kThreads);
   const int smem = KernelShape<false, false>::kSmemBytes;  // the same for every instance
@@ -1729,6 +1745,21 @@ extern "C" sv_status mla_verify_decode_kv8(const void* q_latent, const void* kv_
                          block_table, R, q_per_req, max_pages_per_req, kv_bounds, gate, gate_dim,
                          H, softmax_scale, num_splits, form, workspace, workspace_bytes, out, lse,
                          status, stream);
+}
+
+// Test entry point: the verify attention (bf16 KV, or e4m3 codes with
+// kv_fp8 != 0 and their scale) with the limit of every bounded wait of the
+// attention kernel lowered to wait_ns (the drains at teardown keep theirs).
+extern "C" sv_status sv_test_mla_verify_decode_wait_limit(
+    const void* q_latent, const void* kv_pages, int kv_fp8, float kv_scale, int num_pages, int page_size,
+    const int32_t* block_table, int R, int q_per_req, int max_pages_per_req, const int32_t* kv_bounds,
+    const void* gate, int gate_dim, int H, float softmax_scale, int num_splits, int form, void* workspace,
+    size_t workspace_bytes, void* out, float* lse, int32_t* status, sv_stream_t stream, uint64_t wait_ns) {
+  if (wait_ns > sv::kWaitTimeoutNs) return SV_ERR_SHAPE;  // it only shortens the waits
+  return sv::verify_impl(q_latent, kv_pages, kv_fp8 != 0, kv_fp8 ? kv_scale : 1.0f, num_pages, page_size,
+                         block_table, R, q_per_req, max_pages_per_req, kv_bounds, gate, gate_dim, H,
+                         softmax_scale, num_splits, form, workspace, workspace_bytes, out, lse, status, stream,
+                         wait_ns);
 }
 
 extern "C" sv_status mla_verify_decode(const void* q_latent, const void* kv_pages, int num_pages,

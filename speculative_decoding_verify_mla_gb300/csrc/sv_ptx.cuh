@@ -87,18 +87,50 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
   return ok != 0;
 }
 
+// Non-blocking test of a barrier phase (try_wait above may suspend the
+// thread for a while before it answers no).
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_test_now(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  if constexpr (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on a barrier phase.  Returns false (after setting the abort
-// flag and the status bit) when the wait gives up or when another role of the
-// CTA has already aborted.
+// flag and the status bit) when the wait gives up, i.e. once limit_ns of
+// %globaltimer have passed (a limit of 0: unless the phase has already
+// completed), or when another role of the CTA has already aborted.  With a
+// limit known at compile time to be nonzero the zero case folds away.
 template <bool kCluster>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status) {
+                                          int32_t* status, uint64_t limit_ns = kWaitTimeoutNs) {
+  if (limit_ns == 0) {
+    if (mbar_test_now<kCluster>(bar, parity)) return true;
+    *abort_flag = 1;
+    if (status) atomicOr(status, SV_DEV_TIMEOUT);
+    return false;
+  }
   if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (kCluster ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (globaltimer_ns() - t0 >= limit_ns) {
       *abort_flag = 1;
       if (status) atomicOr(status, SV_DEV_TIMEOUT);
       return false;

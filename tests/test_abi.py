@@ -225,3 +225,21 @@ def test_kv8_host_checks(lib):
     assert f(*a) == 0            # no requests
     a = list(base); a[15] = 9
     assert f(*a) == 5            # unknown kernel form
+
+
+def test_wait_limit_entry_only_shortens_the_waits(lib):
+    """The test entry point with a per-call wait limit refuses a limit above
+    the library's own two seconds before it looks at any other argument
+    (every pointer here is NULL)."""
+    f = lib.sv_test_mla_verify_decode_wait_limit
+    c = ctypes
+    f.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_float, c.c_int, c.c_int, c.c_void_p, c.c_int, c.c_int,
+                  c.c_int, c.c_void_p, c.c_void_p, c.c_int, c.c_int, c.c_float, c.c_int, c.c_int, c.c_void_p,
+                  c.c_size_t, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_uint64]
+    f.restype = c.c_int
+    args = [None, None, 0, 1.0, 4, 64, None, 2, 4, 2, None, None, 512, 8, 0.1, 1, 0, None, 0, None, None, None,
+            None]
+    assert f(*args, 2_000_000_001) == 2  # SV_ERR_SHAPE
+    assert f(*args, (1 << 64) - 1) == 2
+    for limit in (0, 1000, 2_000_000_000):
+        assert f(*args, limit) == 1  # SV_ERR_NULL: the usual checks follow
