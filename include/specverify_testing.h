@@ -48,6 +48,20 @@ sv_status sv_test_mla_verify_decode_wait_limit(const void* q_latent, const void*
                                                size_t workspace_bytes, void* out, float* lse,
                                                int32_t* status, sv_stream_t stream, uint64_t wait_ns);
 
+/* ------------------------------------------------------------------------
+ * sv_test_mla_wuv_project_wait_limit
+ *
+ * mla_wuv_project with every bounded wait of its kernel limited to wait_ns
+ * nanoseconds (0: a wait gives up unless its phase has already completed),
+ * as sv_test_mla_verify_decode_wait_limit above.  When a wait gives up the
+ * kernel sets SV_DEV_TIMEOUT in *status, writes no output row, waits for the
+ * copies and MMAs it started, frees its TMEM and returns.  wait_ns above 2e9
+ * returns SV_ERR_SHAPE; everything else as mla_wuv_project in specverify.h.
+ * ---------------------------------------------------------------------- */
+sv_status sv_test_mla_wuv_project_wait_limit(const void* x, const void* w_uv, int T, int H, int v_dim,
+                                             void* out_v, int32_t* status, sv_stream_t stream,
+                                             uint64_t wait_ns);
+
 #ifdef __cplusplus
 }
 #endif

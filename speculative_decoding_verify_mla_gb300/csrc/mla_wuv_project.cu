@@ -49,10 +49,14 @@ __host__ __device__ constexpr int wuv_smem_bytes(int v_dim) {
   return wuv_stages(v_dim) * wuv_stage_bytes(v_dim) + kWTail + 1024;
 }
 
+// kShortWaits: the test instance, whose bounded waits give up after wait_ns
+// instead of kWaitTimeoutNs.
+template <bool kShortWaits>
 __global__ void __launch_bounds__(kWThreads, 1)
     wuv_project_kernel(const __grid_constant__ CUtensorMap tmap_x,
                        const __grid_constant__ CUtensorMap tmap_w, int T, int H, int v_dim,
-                       __nv_bfloat16* __restrict__ out_v, int32_t* __restrict__ status) {
+                       __nv_bfloat16* __restrict__ out_v, int32_t* __restrict__ status, uint64_t wait_ns) {
+  const uint64_t limit = kShortWaits ? wait_ns : kWaitTimeoutNs;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -96,7 +100,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       int last[kWMaxStages] = {-1, -1, -1, -1, -1, -1, -1, -1};
       for (int c = 0; c < kWChunks; ++c) {
         const int s = c % kWStages, rd = c / kWStages;
-        if (rd > 0 && !mbar_wait<false>(empty(s), (rd - 1) & 1, abort_flag, status)) break;
+        if (rd > 0 && !mbar_wait<false>(empty(s), (rd - 1) & 1, abort_flag, status, limit)) break;
         mbar_arrive_expect_tx(full(s), kWABytes + b_bytes);
         const uint32_t st = sbase + s * kWStageBytes;
         tma_load_3d(st, &tmap_x, full(s), c * 64, h, t0);
@@ -118,7 +122,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     bool ok = true;
     for (int c = 0; ok && c < kWChunks; ++c) {
       const int s = c % kWStages, rd = c / kWStages;
-      ok = mbar_wait<false>(full(s), rd & 1, abort_flag, status);
+      ok = mbar_wait<false>(full(s), rd & 1, abort_flag, status, limit);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -134,20 +138,32 @@ __global__ void __launch_bounds__(kWThreads, 1)
       }
       __syncwarp();
     }
-    if (lane == 0) mma_commit(done);
+    if (lane == 0) {
+      mma_commit(done);
+      // the MMAs issued have completed before the CTA moves on to the
+      // epilogue and frees the TMEM, also when a wait gave up
+      const uint64_t tw = globaltimer_ns();
+      while (!mbar_test(done, 0) && globaltimer_ns() - tw < kWaitTimeoutNs) {
+      }
+    }
     __syncwarp();
   }
 
-  // ---- epilogue: thread i owns token row t0 + i (TMEM lane i)
-  const bool ok = mbar_wait<false>(done, 0, abort_flag, status);
+  // ---- epilogue: thread i owns token row t0 + i (TMEM lane i).  After the
+  // barrier every role has finished: a CTA in which a wait gave up (its
+  // abort flag is set, and the MMAs may not have run) reads no TMEM and
+  // writes nothing.
+  __syncthreads();
+  const bool ok =
+      __all_sync(0xFFFFFFFFu, mbar_wait<false>(done, 0, abort_flag, status, limit) && *abort_flag == 0);
   tc_fence_after();
   const int t = t0 + warp * 32 + lane;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  for (int c0 = 0; c0 < v_dim; c0 += 32) {
+  for (int c0 = 0; ok && c0 < v_dim; c0 += 32) {
     uint32_t v[32];
     tmem_ld32(tmem + lane_off + (uint32_t)c0, v);
     tmem_wait_ld();
-    if (ok && t < T) {
+    if (t < T) {
       uint4* dst = reinterpret_cast<uint4*>(out_v + ((long long)t * H + h) * v_dim + c0);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -171,12 +187,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
 std::mutex g_wuv_mu;
 bool g_wuv_attr[64];
 
-}  // namespace
-}  // namespace sv
-
-extern "C" sv_status mla_wuv_project(const void* x, const void* w_uv, int T, int H, int v_dim,
-                                     void* out_v, int32_t* status, sv_stream_t stream) {
-  using namespace sv;
+sv_status wuv_impl(const void* x, const void* w_uv, int T, int H, int v_dim, void* out_v, int32_t* status,
+                   sv_stream_t stream, uint64_t wait_ns) {
   if (T < 0 || H < 0) return SV_ERR_SHAPE;
   if (v_dim < 32 || v_dim > kWMaxV || v_dim % 32 != 0) return SV_ERR_UNSUPPORTED;
   if (T == 0 || H == 0) return SV_OK;
@@ -190,7 +202,9 @@ extern "C" sv_status mla_wuv_project(const void* x, const void* w_uv, int T, int
   {
     std::lock_guard<std::mutex> lk(g_wuv_mu);
     if (!g_wuv_attr[dev]) {
-      if (cudaFuncSetAttribute(wuv_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(wuv_project_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kWSmemMax) != cudaSuccess ||
+          cudaFuncSetAttribute(wuv_project_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kWSmemMax) != cudaSuccess) {
         cudaGetLastError();
         return SV_ERR_DEVICE;
@@ -208,7 +222,25 @@ extern "C" sv_status mla_wuv_project(const void* x, const void* w_uv, int T, int
       !encode_map(&tmap_w, bf16, 2, w_uv, 3, w_dims, w_box))
     return get_encode_fn() ? SV_ERR_ALIGN : SV_ERR_DEVICE;
   const dim3 grid((unsigned)H, (unsigned)((T + 127) / 128), 1);
-  wuv_project_kernel<<<grid, kWThreads, wuv_smem_bytes(v_dim), reinterpret_cast<cudaStream_t>(stream)>>>(
-      tmap_x, tmap_w, T, H, v_dim, static_cast<__nv_bfloat16*>(out_v), status);
+  auto kernel = wait_ns < kWaitTimeoutNs ? wuv_project_kernel<true> : wuv_project_kernel<false>;
+  kernel<<<grid, kWThreads, wuv_smem_bytes(v_dim), reinterpret_cast<cudaStream_t>(stream)>>>(
+      tmap_x, tmap_w, T, H, v_dim, static_cast<__nv_bfloat16*>(out_v), status, wait_ns);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace sv
+
+extern "C" sv_status mla_wuv_project(const void* x, const void* w_uv, int T, int H, int v_dim,
+                                     void* out_v, int32_t* status, sv_stream_t stream) {
+  return sv::wuv_impl(x, w_uv, T, H, v_dim, out_v, status, stream, sv::kWaitTimeoutNs);
+}
+
+// Test entry point: mla_wuv_project with the limit of every bounded wait of
+// the kernel lowered to wait_ns (the drains before teardown keep theirs).
+extern "C" sv_status sv_test_mla_wuv_project_wait_limit(const void* x, const void* w_uv, int T, int H, int v_dim,
+                                                        void* out_v, int32_t* status, sv_stream_t stream,
+                                                        uint64_t wait_ns) {
+  if (wait_ns > sv::kWaitTimeoutNs) return SV_ERR_SHAPE;  // it only shortens the waits
+  return sv::wuv_impl(x, w_uv, T, H, v_dim, out_v, status, stream, wait_ns);
 }

@@ -243,3 +243,10 @@ def test_wait_limit_entry_only_shortens_the_waits(lib):
     assert f(*args, (1 << 64) - 1) == 2
     for limit in (0, 1000, 2_000_000_000):
         assert f(*args, limit) == 1  # SV_ERR_NULL: the usual checks follow
+    g = lib.sv_test_mla_wuv_project_wait_limit
+    g.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p,
+                  c.c_uint64]
+    g.restype = c.c_int
+    assert g(None, None, 8, 4, 128, None, None, None, 2_000_000_001) == 2  # SV_ERR_SHAPE
+    for limit in (0, 2_000_000_000):
+        assert g(None, None, 8, 4, 128, None, None, None, limit) == 1  # SV_ERR_NULL

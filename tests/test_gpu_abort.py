@@ -14,7 +14,8 @@ kernel instance (bf16 and fp8 KV, two-CTA and stacked forms, one and two
 score issuers) and with the split merge and the balanced plan behind it; and
 a few microseconds on a larger batch, so that CTAs give up at different
 points of their pipelines.  After each such call the device is still usable
-and the next call, with the usual limit, matches the float64 oracle.
+and the next call, with the usual limit, matches the float64 oracle.  The
+per-head W_UV projection kernel gets the same treatment.
 """
 import ctypes
 
@@ -23,8 +24,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import check_attention, device_inputs
-from workloads import fp8_kv_pool, make_inputs, small_config
+from gpu_util import bf16_tensor, check_attention, device_inputs, to_f64
+from workloads import f32_to_bf16_bits, fp8_kv_pool, make_inputs, small_config
 
 pytestmark = pytest.mark.gpu
 
@@ -45,6 +46,10 @@ def sv():
                   c.c_int, c.c_void_p, c.c_void_p, c.c_int, c.c_int, c.c_float, c.c_int, c.c_int, c.c_void_p,
                   c.c_size_t, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_uint64]
     f.restype = c.c_int
+    g = lib.sv_test_mla_wuv_project_wait_limit
+    g.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p,
+                  c.c_uint64]
+    g.restype = c.c_int
     return m
 
 
@@ -118,3 +123,34 @@ def test_waits_give_up_mid_pipeline_on_a_wave_batch(sv, limit_ns):
     assert st == 0, f"status {st:#x}"
     ref_o, ref_l = _oracle(inp, 0)
     check_attention(out, lse, ref_o, ref_l, label=f"wave batch after a {limit_ns} ns limit")
+
+
+@pytest.mark.parametrize("T,H,V", [(160, 4, 128), (40, 3, 256)])
+def test_wuv_wait_runs_out_then_next_call_is_exact(sv, T, H, V):
+    """The W_UV projection: with a zero limit every CTA's first wait for a
+    copy gives up; the kernel writes no output row (the NaN fill stays) and
+    returns; the next call is exact."""
+    rng = np.random.default_rng(T + H + V)
+    x = f32_to_bf16_bits(rng.standard_normal((T, H, 512), dtype=np.float32))
+    w = f32_to_bf16_bits(rng.standard_normal((H, V, 512), dtype=np.float32) / np.float32(16.0))
+    xd, wd = bf16_tensor(x, DEV), bf16_tensor(w, DEV)
+    f = sv.load_library().sv_test_mla_wuv_project_wait_limit
+
+    def call(limit):
+        out = torch.full((T, H, V), float("nan"), dtype=torch.bfloat16, device=DEV)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        rc = f(xd.data_ptr(), wd.data_ptr(), T, H, V, out.data_ptr(), status.data_ptr(),
+               torch.cuda.current_stream().cuda_stream, limit)
+        assert rc == 0, rc
+        torch.cuda.synchronize()
+        return out, int(status.item())
+
+    out, st = call(0)
+    assert st == SV_DEV_TIMEOUT, f"status {st:#x}"
+    assert torch.isnan(out.float()).all()  # every CTA gave up and wrote nothing
+    out, st = call(USUAL_LIMIT_NS)
+    assert st == 0, f"status {st:#x}"
+    ref = oracle.ref_wuv_project(x, w)
+    g = to_f64(out)
+    rel = np.linalg.norm(g - ref) / np.linalg.norm(ref)
+    assert rel <= 5e-3, f"W_UV after abort: rel-L2 {rel:.3e}"  # bf16 output rounding, as the W_UV parity
