@@ -324,7 +324,8 @@ __device__ __forceinline__ void store_boxes(const EpilogueCtx& c, int bx0, int b
           if (c.fused)
             tma_store_3d(c.tmap_out, src, h * kDHalf + bx * 64, 0, c.r);
           else
-            tma_store_4d(c.tmap_part, src, h * kDHalf + bx * 64, 0, c.r, c.s_idx);
+            tma_store_4d(c.tmap_part, src, h * kDHalf + bx * 64, 0, (c.p->units || c.p->wave_s > 0) ? 0 : c.r,
+                         (c.p->units || c.p->wave_s > 0) ? c.slot : c.s_idx);
         }
       }
       tma_store_commit();
@@ -1026,7 +1027,7 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
             if (fused)
               tma_store_3d(&tmap_out, src, h * kDHalf + bx * 64, 0, r);
             else
-              tma_store_4d(&tmap_part, src, h * kDHalf + bx * 64, 0, r, s_idx);
+              tma_store_4d(&tmap_part, src, h * kDHalf + bx * 64, 0, slotted ? 0 : r, slotted ? slot : s_idx);
           }
         }
         tma_store_commit();
@@ -1162,18 +1163,21 @@ __global__ void __launch_bounds__(KernelShape<kF8, kTwo>::kThreads, 1)
 
 // ------------------------------------------------------------------ balanced plan
 // One CTA turns the per-token bounds into the unit list of the attention
-// kernel.  Request r needs n_r = ceil(max_t b_t / 64) KV tiles; with n_mt row
-// tiles per request and two latent halves, the whole batch is
-// 2 * n_mt * sum_r n_r CTA-tiles of work.  Pieces of c tiles,
-//   c = max(ceil(sum_r n_r * n_mt / SMs), ceil(max_r n_r / SV_MAX_SPLITS)),
-// give about two units per SM; request r gets s_r = max(1, ceil(n_r / c))
+// kernel.  Request r needs n_r = ceil(max_t b_t / 64) KV tiles; a piece of a
+// request is `upp` units (two-CTA form: n_mt row tiles x two latent halves;
+// stacked form: one CTA), so the whole batch is upp * sum_r n_r CTA-tiles of
+// work.  Pieces of c tiles,
+//   c = max(ceil(sum_r n_r * wm / (SMs * wd)), ceil(max_r n_r / SV_MAX_SPLITS)),
+// with wm = n_mt, wd = 1 (two-CTA: about two units per SM) or wm = 1, wd =
+// kStackPlanDiv (stacked: about one unit per SM, whose units are short and
+// pay their fixed cost once); request r gets s_r = max(1, ceil(n_r / c))
 // pieces (the last one shorter).  Units are listed longest first (a counting
 // sort over piece lengths), so the block scheduler hands the long pieces out
 // before the short ones.  A request with one piece is finished by its units
 // (normalise + gate); the others write partials to slots plan_base[r] + j.
 // Layout of the plan area: header {c, n_units, n_slots}, splits[R],
-// base[R], units[units_max] (int4: r, m_tile << 1 | half, lo | hi << 16,
-// slot or -1).
+// base[R], units[units_max] (int4: r, m_tile << 1 | half (stacked: 0),
+// lo | hi << 16, slot or -1).
 constexpr int kPlanThreads = 1024;
 constexpr int kLenBuckets = 1024;
 
@@ -1236,7 +1240,7 @@ __device__ int block_excl_scan(int v, int* s_scan, int* total) {
 
 __global__ void __launch_bounds__(kPlanThreads)
     plan_kernel(const int32_t* __restrict__ kv_bounds, int R, int q_per_req, int max_pages,
-                int n_mt, int sms, int units_max, int slots_max, int* __restrict__ header,
+                int upp, int wm, int wd, int sms, int units_max, int slots_max, int* __restrict__ header,
                 int* __restrict__ splits, int* __restrict__ base, int4* __restrict__ units,
                 int32_t* __restrict__ status) {
   __shared__ long long s_red64[32];
@@ -1260,7 +1264,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   }
   psum = block_reduce<long long>(psum, s_red64, false);
   pmax = block_reduce<int>(pmax, s_red, true);
-  long long c = (psum * n_mt + sms - 1) / sms;
+  long long c = (psum * wm + (long long)sms * wd - 1) / ((long long)sms * wd);
   c = max(c, (long long)(pmax + SV_MAX_SPLITS - 1) / SV_MAX_SPLITS);
   if (c < 1) c = 1;
   // 2. pieces per request, slots, and piece-length histogram
@@ -1276,7 +1280,7 @@ __global__ void __launch_bounds__(kPlanThreads)
       for (int j = 0; j < sr; ++j) {
         const int len = (j < sr - 1) ? (int)c : n - (int)((sr - 1) * c);
         const int bk = (int)((long long)len * (kLenBuckets - 1) / c);
-        atomicAdd(&s_cnt[bk], 2 * n_mt);
+        atomicAdd(&s_cnt[bk], upp);
       }
     }
     int tot = 0;
@@ -1285,7 +1289,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     carry_slots += tot;
     int tu = 0;
     block_excl_scan(sr, s_scan, &tu);
-    carry_units += tu * 2 * n_mt;
+    carry_units += tu * upp;
   }
   __syncthreads();
   // 3. start of every length bucket, longest first (bucket kLenBuckets-1 first)
@@ -1307,17 +1311,19 @@ __global__ void __launch_bounds__(kPlanThreads)
       const int plo = (int)(j * c);
       const int phi = (j < sr - 1) ? (int)((j + 1) * c) : n;
       const int bk = (int)((long long)(phi - plo) * (kLenBuckets - 1) / c);
-      const int pos = atomicAdd(&s_cnt[bk], 2 * n_mt);
+      const int pos = atomicAdd(&s_cnt[bk], upp);
       const int sl = sr >= 2 ? base[r] + j : -1;
-      for (int u = 0; u < 2 * n_mt; ++u)
+      for (int u = 0; u < upp; ++u)
         if (SV_DCHECK(pos + u >= 0 && pos + u < units_max && sl < slots_max, status))
           units[pos + u] = make_int4(r, u, plo | (phi << 16), sl);
     }
   }
   __syncthreads();
+  // a plan that does not fit the plan area (reported above) places no unit
+  // and leaves every request at one piece, so the merge reads no slot
   for (int r = tid; r < R; r += kPlanThreads) {
     const int n = splits[r];
-    splits[r] = n == 0 ? 1 : (int)((n + c - 1) / c);
+    splits[r] = (n == 0 || !fits) ? 1 : (int)((n + c - 1) / c);
   }
   if (tid == 0) {
     header[0] = (int)c;
@@ -1376,6 +1382,17 @@ inline bool use_stack(long long Mq, long long max_pages, long long S, int form) 
   if (Mq > 64 || form == SV_FORM_TWO_CTA) return false;
   return form == SV_FORM_STACKED || (max_pages + S - 1) / S >= kStackMinTiles;
 }
+// The same under the balanced plan, whose pieces hold ceil(sum n_r / SMs)
+// tiles or more (the stacked form's units are one per SM).
+inline bool use_stack_balanced(long long Mq, int form) { return Mq <= 64 && form != SV_FORM_TWO_CTA; }
+// Stacked units per SM the balanced plan aims at (pieces of
+// ceil(sum n_r / (SMs * kStackPlanDiv)) tiles).  plan_layout and
+// plan_workspace_bound hold at most kStackPlanDiv * SMs + R + 1 pieces.
+// Measured on 16 plain-decode requests of 8K-32K positions (GB300): one
+// unit per SM 99-100 us, two 116 us, the two-CTA form's plan 122 us.
+// (Raising c further until every unit fits one wave measured slower.)
+constexpr int kStackPlanDiv = 1;
+static_assert(kStackPlanDiv >= 1 && kStackPlanDiv <= 2, "the plan area is sized for at most two units per SM");
 
 // Splits: enough (request, row tile, split, latent half) CTAs to fill the SMs
 // once, each split keeping at least 2 KV tiles (on the C = 1 verify batch,
@@ -1442,10 +1459,12 @@ struct PlanLayout {
   size_t splits, base, units, part_o, part_lse, total;
   int units_max, slots_max;
 };
-PlanLayout plan_layout(int R, int Mq, int n_mt, int sms) {
+PlanLayout plan_layout(int R, int Mq, int n_mt, int sms, bool stack) {
   PlanLayout L;
-  L.units_max = 2 * sms + 2 * n_mt * R;
-  L.slots_max = sms / n_mt + R + 1;
+  // two-CTA pieces: sum_r s_r <= sum n_r / c + R <= SMs / n_mt + R, 2 n_mt
+  // units each; stacked pieces: <= kStackPlanDiv SMs + R, one unit each
+  L.units_max = stack ? kStackPlanDiv * sms + R + 1 : 2 * sms + 2 * n_mt * R;
+  L.slots_max = stack ? kStackPlanDiv * sms + R + 1 : sms / n_mt + R + 1;
   L.splits = 256;
   L.base = L.splits + align256((size_t)R * 4);
   L.units = L.base + align256((size_t)R * 4);
@@ -1455,7 +1474,9 @@ PlanLayout plan_layout(int R, int Mq, int n_mt, int sms) {
   return L;
 }
 // An upper bound of plan_layout(...).total from T = R*q_per_req and H only
-// (n_mt * R <= T*H/128 + R, slots * Mq <= 128*sms + 2*T*H).
+// (two-CTA: n_mt * R <= T*H/128 + R, slots * Mq <= 128*sms + 2*T*H; stacked,
+// Mq <= 64: pieces <= 2*sms + R + 1 <= 2*sms + 2*T, slots * Mq <= 128*sms +
+// 2*T*H).
 size_t plan_workspace_bound(long long T, long long H, int sms) {
   const long long rows = T * H;
   const long long units_max = 2ll * sms + 2 * (rows / 128 + T);
@@ -1547,6 +1568,10 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   int wave_k = 0, wave_s = 0;
   if (wave && !wave_params(R, n_mt, max_pages_per_req, sm_count, &wave_k, &wave_s)) return SV_ERR_SHAPE;
   const long long wave_slots = (long long)(R - wave_k) * wave_s;
+  // stacked instance: requests of <= 64 query rows, uniform splits or the
+  // balanced plan; its row maps have 64-row boxes
+  const bool stack = !wave && (balanced ? use_stack_balanced(Mq_ll, form)
+                                        : use_stack(Mq_ll, max_pages_per_req, S, form));
   __nv_bfloat16* part_o = nullptr;
   float* part_lse = nullptr;
   PlanLayout PL{};
@@ -1554,7 +1579,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   if (balanced) {
     if (!workspace) return SV_ERR_WORKSPACE;
     if (misaligned(workspace, 256)) return SV_ERR_ALIGN;
-    PL = plan_layout(R, (int)Mq_ll, n_mt, sm_count);
+    PL = plan_layout(R, (int)Mq_ll, n_mt, sm_count, stack);
     if (workspace_bytes < PL.total ||
         workspace_bytes < sv_mla_verify_workspace_bytes((int)T, H, SV_SPLITS_BALANCED))
       return SV_ERR_WORKSPACE;
@@ -1577,9 +1602,6 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   }
   if (!get_encode_fn()) return SV_ERR_DEVICE;
   const long long Mq = (long long)H * q_per_req;
-  // stacked instance: requests of <= 64 query rows, uniform splits; its row
-  // maps have 64-row boxes
-  const bool stack = !balanced && !wave && use_stack(Mq, max_pages_per_req, S, form);
   const int m_box = stack ? 64 : kMTile;
   CUtensorMap tmap_kv, tmap_q, tmap_gate, tmap_out, tmap_part;
   {
@@ -1599,7 +1621,7 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
     if (balanced || wave) {
       const cuuint64_t slots = balanced ? (cuuint64_t)PL.slots_max : (cuuint64_t)wave_slots;
       const cuuint64_t part_dims[4] = {(cuuint64_t)kD, (cuuint64_t)Mq, 1, slots};
-      const cuuint32_t part_box[4] = {64, (cuuint32_t)kMTile, 1, 1};
+      const cuuint32_t part_box[4] = {64, (cuuint32_t)m_box, 1, 1};
       if (!encode_map(&tmap_part, bf16, 2, part_o, 4, part_dims, part_box))
         return SV_ERR_ALIGN;
     } else if (S > 1) {
@@ -1689,9 +1711,10 @@ sv_status verify_impl(const void* q_latent, const void* kv_pages, bool kv_fp8, f
   int* splits = reinterpret_cast<int*>(plan_base_ptr + PL.splits);
   int* pbase = reinterpret_cast<int*>(plan_base_ptr + PL.base);
   int4* units = reinterpret_cast<int4*>(plan_base_ptr + PL.units);
-  plan_kernel<<<1, kPlanThreads, 0, st>>>(kv_bounds, R, q_per_req, max_pages_per_req, n_mt,
-                                          sm_count, PL.units_max, PL.slots_max, header, splits,
-                                          pbase, units, status);
+  plan_kernel<<<1, kPlanThreads, 0, st>>>(kv_bounds, R, q_per_req, max_pages_per_req,
+                                          stack ? 1 : 2 * n_mt, stack ? 1 : n_mt, stack ? kStackPlanDiv : 1, sm_count,
+                                          PL.units_max, PL.slots_max, header, splits, pbase, units,
+                                          status);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_LAUNCH;
   prm.units = units;
   prm.plan_header = header;

@@ -57,6 +57,17 @@ def test_kv8_splits_and_plan(sv, splits):
     check_attention(out, lse, ref_o, ref_l, label=f"kv8 splits={splits}")
 
 
+@pytest.mark.parametrize("splits", [2, -1])
+def test_kv8_stacked_splits_and_plan(sv, splits):
+    """The fp8 stacked form (M = 64 rows per request) under uniform splits and
+    the balanced plan, ragged contexts."""
+    cfg = small_config("c3", R=5, k=0, H=64, kv_lens=(70, 1900, 333, 64, 1200), kv_len_range=None, shuffled=True,
+                       vocab=64)
+    inp = make_inputs(cfg, seed=51)
+    out, lse, ref_o, ref_l = _run(sv, inp, splits, form=sv.FORM_STACKED)
+    check_attention(out, lse, ref_o, ref_l, label=f"kv8 stacked splits={splits}")
+
+
 @pytest.mark.parametrize("mode", ["always", "off"])
 @pytest.mark.parametrize("H,k,lens", [(64, 0, (1100, 64, 4, 700)), (16, 3, (333, 65, 4)), (8, 3, (64, 100))])
 def test_kv8_stacked_form(sv, mode, H, k, lens):

@@ -1,7 +1,7 @@
 """GPU parity of the stacked attention form (requests of at most 64 query
 rows on one CTA that holds both latent halves) against the float64 oracle,
 with the form chosen per call (forced on, forced off, automatic) on the same
-inputs (C ABI calls)."""
+inputs, under uniform splits and the balanced plan (C ABI calls)."""
 import numpy as np
 import pytest
 import torch
@@ -65,7 +65,7 @@ def test_stacked_matches_oracle(sv, H, k, lens, on):
     cfg = small_config("c0", R=len(lens), k=k, H=H, kv_lens=lens, shuffled=True, vocab=64)
     inp = make_inputs(cfg, seed=11)
     ref_o, ref_l = _oracle(inp)
-    for splits in (1, 2, 5, 0):
+    for splits in (1, 2, 5, 0, sv.SV_SPLITS_BALANCED):
         out, lse = _attention(sv, inp, splits, form=form_of(sv, on))
         check_attention(out, lse, ref_o, ref_l, label=f"stacked={on} H={H} k={k} splits={splits}")
 
@@ -86,7 +86,7 @@ def test_stacked_zero_bounds_nan_slack_headwise_gate(sv):
     ref_o, ref_l = _oracle(inp, bounds=bounds, kv_bits=kv)
     g_head = np.ascontiguousarray(inp["gate_bits"][:, :, 0])
     ref_oh, ref_lh = _oracle(inp, bounds=bounds, kv_bits=kv, gate_bits=g_head)
-    for splits in (1, 4):
+    for splits in (1, 4, sv.SV_SPLITS_BALANCED):
         out, lse = _attention(sv, inp, splits, bounds=bounds, kv_bits=kv, form=sv.FORM_STACKED)
         check_attention(out, lse, ref_o, ref_l, label=f"zero bounds + nan slack, splits={splits}")
         out, lse = _attention(sv, inp, splits, bounds=bounds, kv_bits=kv, gate_bits=g_head, form=sv.FORM_STACKED)
@@ -149,3 +149,27 @@ def test_auto_splits_count_one_cta_per_unit(sv):
     assert s_auto == max(1, min(sms // 64, 12))
     assert s_off == max(1, min(sms // 128, 12))
     assert s_short == 1
+
+
+def test_stacked_balanced_plan_c3(sv):
+    """The C = 64 plain-decode batch (64 requests x 16-24 KV tiles) in the
+    stacked form under the balanced plan (pieces of ceil(sum n_r / SMs)
+    tiles, one CTA each, partials merged per request), and the two-CTA form
+    under the same plan, against the oracle over every token and head."""
+    inp = make_inputs("c3", seed=0)
+    ref_o, ref_l = _oracle(inp)
+    for form in (sv.FORM_STACKED, sv.FORM_TWO_CTA):
+        out, lse = _attention(sv, inp, sv.SV_SPLITS_BALANCED, form=form)
+        check_attention(out, lse, ref_o, ref_l, label=f"c3 balanced plan, form={form}")
+
+
+def test_stacked_balanced_plan_long_context(sv):
+    """Plain decode at long context (16 requests of 8K-32K positions, k = 0,
+    H = 64: 64 rows per request, 10% zero bounds): the automatic choice is
+    the balanced plan in the stacked form; every token and head against the
+    oracle."""
+    inp = make_inputs(small_config("c4", k=0), seed=0)
+    assert sv.num_splits_for(inp["R"], 1, 64, inp["max_pages"]) == sv.SV_SPLITS_BALANCED
+    ref_o, ref_l = _oracle(inp)
+    out, lse = _attention(sv, inp, 0)
+    check_attention(out, lse, ref_o, ref_l, label="long-context plain decode, balanced plan, stacked")
