@@ -46,7 +46,7 @@ def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="c4")
     ap.add_argument("--extra-configs", default="c1,c2,c3",
                     help="comma-separated configurations measured after the main one ('' for none)")

@@ -196,7 +196,12 @@ int greedy_chunk(int T, int V) {
   const long long total = (long long)T * V;
   long long c = (total + 12 * 152 - 1) / (12 * 152);  // about twelve CTAs per SM
   c = (c + 8191) / 8192 * 8192;
-  if (c < 8192) c = 8192;
+  // CTAs of at least 64 KB when the logits can fill four of them per SM:
+  // 32 KB CTAs take one round of loads per thread and pay the per-CTA key
+  // atomic and ticket for little streaming (the C = 64 decode call 16.2 ->
+  // 14.5 us; smaller batches keep 32 KB chunks to spread over the SMs)
+  const long long cmin = total >= 4ll * 152 * 16384 ? 16384 : 8192;
+  if (c < cmin) c = cmin;
   if (c > 65536) c = 65536;
   return (int)c;
 }
