@@ -1,7 +1,7 @@
 """A seeded sweep of the attention over shapes and modes, against the
 float64 oracle.
 
-Every case draws a batch (1-12 requests, k = 0-9, H from 1 to 128, context
+Every attention case draws a batch (1-12 requests, k = 0-9, H from 1 to 128, context
 lengths from 1 to 2500 positions, shuffled block tables), sets about 10% of
 the tokens' bounds to 0 (the (-inf, 0) rows of "TensorRT-LLM PR #18166: Kimi
 K3 DSpark speculative decoding under Helix CP", zero-bound commit messages)
@@ -10,7 +10,8 @@ runs the kernel under three (split mode, kernel form) choices drawn from
 uniform splits, the balanced plan and the automatic choice, and the two-CTA,
 stacked and automatic forms, with bf16 or fp8 KV and the elementwise or
 head-wise gate.  Two more batches sit in the wave split mode's range.  The
-cases come from a fixed seed, so a failure names a reproducible case.
+greedy verify gets the same treatment over shapes and tie patterns.  The
+cases come from fixed seeds, so a failure names a reproducible case.
 """
 import numpy as np
 import pytest
@@ -134,3 +135,39 @@ def test_sweep_wave_mode(sv, fp8):
     ref = oracle.ref_verify_attention(inp["q_bits"], kv_ref, inp["block_table"], bounds, inp["gate_bits"], 5,
                                       inp["softmax_scale"])
     check_attention(out, lse, *ref, label=f"wave mode fp8={fp8}")
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_sweep_greedy(sv, i):
+    """Greedy verify on seeded shapes (1-40 requests, k = 0-12, V from 1 to
+    200003, odd and even), logits drawn from a few integer levels so that
+    the row maxima repeat (ties across threads, chunks and CTAs; signed
+    zeros), drafts that follow the argmax chain for a random number of steps
+    then differ: bit for bit against the oracle, twice in a row (the second
+    call checks that the first left its workspace clean)."""
+    rng = np.random.default_rng(5000 + i)
+    R = int(rng.integers(1, 41))
+    k = int(rng.integers(0, 13))
+    V = int(rng.choice([1, 2, 3, 5, 64, 1000, 4097, 8192, 16385, 65536, 163840, 200003]))
+    while R * (k + 1) * V > 20_000_000:
+        R = max(1, R // 2)
+    T = R * (k + 1)
+    levels = np.array([-3.0, -0.0, 0.0, 1.5, 2.0], dtype=np.float32)
+    x = levels[rng.integers(0, len(levels), size=(T, V))]
+    a_ref = np.argmax(x, axis=1)  # numpy picks the first maximum (ties, and -0 == +0)
+    drafts = np.zeros((R, k), dtype=np.int32)
+    for r in range(R):
+        n_match = int(rng.integers(0, k + 1))
+        for j in range(k):
+            a = int(a_ref[r * (k + 1) + j])
+            drafts[r, j] = a if j < n_match else (a + 1 + int(rng.integers(0, max(1, V - 1)))) % V
+    kv_in = rng.integers(k + 1, 5000, size=R).astype(np.int32)
+    ref = oracle.ref_greedy_verify(x, drafts, kv_in, k)
+    lt = torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+    dt = torch.from_numpy(drafts).to(DEV)
+    kt = torch.from_numpy(kv_in).to(DEV)
+    ws = torch.zeros(sv.greedy_workspace_bytes(T, V), dtype=torch.uint8, device=DEV)
+    for _ in range(2):
+        got = [t.cpu().numpy() for t in sv.spec_verify_greedy(lt, dt, kt, k, workspace=ws)]
+        for g, r in zip(got, ref):
+            assert np.array_equal(g, np.asarray(r)), f"case {i}: R={R} k={k} V={V}"
