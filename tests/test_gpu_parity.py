@@ -196,6 +196,25 @@ def test_attention_split_sweep(sv, splits):
     check_attention(out, lse, ref_o, ref_l, label=f"splits={splits}")
 
 
+def test_attention_longest_context(sv):
+    """One request of 131072 positions (2048 KV tiles, k = 3, H = 16: 64
+    rows): the automatic uniform split, and the balanced plan in both forms,
+    where the piece length reaches its lower bound ceil(n_r / SV_MAX_SPLITS)
+    (64 pieces of 32 tiles); every token and head against the oracle."""
+    cfg = small_config("c0", R=1, k=3, H=16, kv_lens=(131072,), kv_len_range=None, shuffled=True, vocab=64)
+    inp = make_inputs(cfg, seed=7)
+    ref_o, ref_l = oracle_attention(inp)
+    d = device_inputs(inp, DEV)
+    for splits, form in ((0, sv.FORM_AUTO), (sv.SV_SPLITS_BALANCED, sv.FORM_STACKED),
+                         (sv.SV_SPLITS_BALANCED, sv.FORM_TWO_CTA)):
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        out, lse = sv.mla_verify_decode(d["q"], d["kv"], d["block_table"], d["kv_bounds"], d["gate"], 4,
+                                        inp["softmax_scale"], num_splits=splits, status=status, form=form)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        check_attention(out, lse, ref_o, ref_l, label=f"131072 positions, splits={splits}, form={form}")
+
+
 def test_attention_wave_mode(sv):
     """The wave split mode (the first k requests whole, the others in s
     pieces) on 30 requests x 3 row tiles x 2 halves = 180 CTAs: ragged
@@ -286,7 +305,7 @@ def test_nan_in_pool_slack_does_not_leak(sv):
 
 
 @pytest.mark.parametrize("H,k,lens", [(96, 1, (300, 129)), (1, 0, (65, 1, 640)), (8, 19, (500,)), (64, 7, (64,)),
-                                      (3, 40, (700, 300)), (8, 35, (900,))])
+                                      (3, 40, (700, 300)), (8, 35, (900,)), (128, 15, (1500, 700))])
 def test_attention_head_and_group_shapes(sv, H, k, lens):
     cfg = small_config("c0", R=len(lens), k=k, H=H, kv_lens=lens, shuffled=True, vocab=64)
     inp = make_inputs(cfg, seed=6)
