@@ -122,9 +122,14 @@ const char* sv_status_string(sv_status s);
  *                 SV_SPLITS_BALANCED (-1): a plan computed on the device from
  *                   kv_bounds cuts every request into pieces of c pages,
  *                   c = max(ceil(sum_r n_r * n_tiles / SMs), ceil(max_r n_r / 64))
- *                   (n_tiles = 128-row tiles per request), so that requests of
- *                   very different lengths give the SMs equal work; the
- *                   pieces run longest first.  One extra small kernel.
+ *                   (n_tiles = 128-row tiles per request; two CTAs per
+ *                   128-row tile and piece: about two CTAs per SM), or in
+ *                   the stacked form (one CTA per piece)
+ *                   c = max(ceil(sum_r n_r / SMs), ceil(max_r n_r / 64)), so
+ *                   that requests of very different lengths give the SMs
+ *                   equal work; the pieces run longest first.  One extra
+ *                   small kernel.  A plan that does not fit the workspace
+ *                   sets SV_DEV_BAD_BOUND and computes nothing.
  *                 SV_SPLITS_WAVE (-2): for batches whose 2 * n_tiles * R
  *                   CTAs fill the SMs more than once but less than twice:
  *                   requests 0..k-1 are not split and fill the first wave,
@@ -156,18 +161,20 @@ const char* sv_status_string(sv_status s);
 /* The kernel form of the attention call, chosen per call (the `form`
  * argument of mla_verify_decode_gated / _kv8 and sv_mla_verify_num_splits;
  * mla_verify_decode uses SV_FORM_AUTO).  The stacked form runs requests of
- * M = H*q_per_req <= 64 query rows with uniform splits on one CTA per
- * (request, split): rows 64..127 of the CTA's 128-row MMA tile repeat rows
+ * M = H*q_per_req <= 64 query rows with uniform splits or the balanced plan
+ * on one CTA per (request, split or piece): rows 64..127 of the CTA's
+ * 128-row MMA tile repeat rows
  * 0..63, and the softmax weights P form a block-diagonal operand over the KV
  * tile taken twice, so TMEM lanes 0..63 accumulate latent columns 0..255 and
  * lanes 64..127 columns 256..511 (no second CTA recomputing the scores).
  * The result is the same beyond rounding.
- *   SV_FORM_AUTO      the stacked form when M <= 64, the splits are uniform
- *                     and a unit holds at least 4 KV tiles
+ *   SV_FORM_AUTO      the stacked form when M <= 64 and either the
+ *                     balanced plan runs or the splits are uniform and a
+ *                     unit holds at least 4 KV tiles
  *                     (ceil(max_pages_per_req / S) >= 4); else two CTAs.
  *   SV_FORM_TWO_CTA   always two CTAs per unit, one per latent half.
  *   SV_FORM_STACKED   the stacked form whenever M <= 64 and the splits are
- *                     uniform (else two CTAs).
+ *                     uniform or balanced (else two CTAs).
  * Any other value: SV_ERR_UNSUPPORTED (sv_mla_verify_num_splits returns 0). */
 #define SV_FORM_AUTO 0
 #define SV_FORM_TWO_CTA 1
