@@ -4,9 +4,10 @@ TMEM and global index and every TMA / MMA operand address is checked before
 its access, a failed check sets SV_DEV_DEBUG_CHECK in the status word and
 prints its line.  This is the stand-in for a memory checker: the GPU parity
 tests of the attention (bf16 and fp8 KV, both kernel forms, uniform splits
-and the balanced plan, the gates, the literal entry point) run again in a
-child process that loads the debug library, and must pass with no check
-failing.  The full-size long-context cases are left out for time."""
+and the balanced plan, the gates, the literal entry point, the seeded sweep)
+and the tests that make bounded waits give up run again in a child process
+that loads the debug library, and must pass with no check failing.  The
+full-size long-context cases are left out for time."""
 import os
 import subprocess
 import sys
@@ -19,7 +20,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 FILES = ["tests/test_gpu_parity.py", "tests/test_gpu_stacked.py", "tests/test_gpu_kv8.py",
-         "tests/test_gpu_f4.py", "tests/test_gpu_abi_entry.py"]
+         "tests/test_gpu_f4.py", "tests/test_gpu_abi_entry.py", "tests/test_gpu_sweep.py",
+         "tests/test_gpu_abort.py"]
 
 
 def test_parity_under_the_index_checking_build():
