@@ -563,6 +563,10 @@ def main():
     R, k, H, T, V = m["R"], m["k"], m["H"], m["T"], m["V"]
     roof = dict(main_sum["attention_roofline"])
     roof["traffic"] = recorded_traffic(args.config)
+    if roof["traffic"] is not None:
+        roof["traffic_scope"] = ("dram__bytes_read.sum + dram__bytes_write.sum of the attention kernel "
+                                 "(mla_verify_kernel) per launch, one ncu capture "
+                                 f"(profiles/mla_verify_kernel_{args.config}.md)")
     roof["kernel"] = "mla_verify_decode call (" + {3: "plan + attention + LSE combine kernels",
                                                    2: "attention + LSE combine kernels",
                                                    1: "attention kernel"}[m["attention_launches"]] + ")"
