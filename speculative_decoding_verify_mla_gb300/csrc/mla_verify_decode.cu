@@ -48,7 +48,9 @@
 //    and MMA issuers) and take boxes 2..3 of every row.
 //  * Work units.  Uniform splits decode the unit from blockIdx; the balanced
 //    plan (a one-CTA plan kernel, this grid its programmatic dependent) hands
-//    each CTA a unit of a list ordered longest first.
+//    each CTA a unit of a list ordered longest first; the wave split mode
+//    decodes it in closed form (the first k requests whole, the others in s
+//    pieces, for batches between one and two waves of the SMs).
 //  * MMA issue.  Separate issuing warps for the scores and for P V (and, in
 //    the long-unit instances, a second score warp for the odd tiles), so
 //    the tensor pipe is fed from several warps; each ring slot's descriptor
@@ -56,7 +58,7 @@
 //  * Set-up.  One pass over the request's kv_bounds gives the tile's and the
 //    request's KV extent (an out-of-range bound is reported once, after the
 //    loads, so that they overlap).
-//  * Stacked instance (M <= 64 query rows, uniform splits).  One
+//  * Stacked instance (M <= 64 query rows, uniform splits or the plan).  One
 //    CTA holds both latent halves: rows 64..127 of its 128-row tile repeat
 //    rows 0..63 (the other query half is TMA-loaded twice), so score rows L
 //    and L + 64 are equal; the softmax writes P block-diagonally ([P | 0] in
@@ -68,8 +70,10 @@
 //    issuers: warp 1 the (even tiles') scores, warp 6 P V and, in the
 //    long-unit instances, warp 7 the odd tiles' scores (fp8 KV: P V warp 10,
 //    odd-tile warp 11; its warps 6-9 convert the KV).  Template instances:
-//    KV format x one or two score warps x two-CTA or stacked form.
-//    Every wait is bounded; nothing traps.
+//    KV format x one or two score warps x two-CTA or stacked form, each also
+//    built with a per-launch wait limit for tests.
+//    Every wait is bounded (a wait that gives up sets SV_DEV_TIMEOUT, and
+//    the CTA drains what it started and frees its TMEM); nothing traps.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
