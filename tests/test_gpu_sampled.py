@@ -206,3 +206,23 @@ def test_sampled_invalid_draft_rejected(sv):
     inp["draft_tokens"][1, 0] = -3
     ga, gn, gkv = run_gpu(sv, inp)
     assert list(ga) == [1, 0, k, k]
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_sampled_sweep(sv, i):
+    """Seeded shapes (1-48 requests, k = 0-12, V from 1 to 163840, odd and
+    even), temperatures from 0.3 to 3 and draft mixes from nearly one-hot to
+    nearly uniform, under the same decision and draw rules."""
+    rng = np.random.default_rng(7000 + i)
+    R = int(rng.integers(1, 49))
+    k = int(rng.integers(0, 13))
+    V = int(rng.choice([1, 2, 7, 64, 1000, 4097, 16384, 65536, 163840]))
+    while R * (k + 1) * V > 12_000_000:
+        R = max(1, R // 2)
+    temperature = float(np.exp(rng.uniform(np.log(0.3), np.log(3.0))))
+    lo = float(rng.uniform(0.0, 0.9))
+    mix = (lo, float(min(1.0, lo + rng.uniform(0.05, 0.5))))
+    cfg = small_config("c0", R=R, k=k, vocab=V, kv_lens=None, kv_len_range=(k + 1, 4000))
+    inp = make_sampled_inputs(cfg, seed=8000 + i, temperature=temperature, draft_mix=mix)
+    got = run_gpu(sv, inp)
+    check_sampled(inp, got, max_ambiguous_frac=0.25)
