@@ -10,8 +10,9 @@ runs the kernel under three (split mode, kernel form) choices drawn from
 uniform splits, the balanced plan and the automatic choice, and the two-CTA,
 stacked and automatic forms, with bf16 or fp8 KV and the elementwise or
 head-wise gate.  Two more batches sit in the wave split mode's range.  The
-greedy verify gets the same treatment over shapes and tie patterns.  The
-cases come from fixed seeds, so a failure names a reproducible case.
+greedy verify gets the same treatment over shapes and tie patterns, and
+the paged KV append over batch shapes and skipped tokens.  The cases come
+from fixed seeds, so a failure names a reproducible case.
 """
 import numpy as np
 import pytest
@@ -171,3 +172,33 @@ def test_sweep_greedy(sv, i):
         got = [t.cpu().numpy() for t in sv.spec_verify_greedy(lt, dt, kt, k, workspace=ws)]
         for g, r in zip(got, ref):
             assert np.array_equal(g, np.asarray(r)), f"case {i}: R={R} k={k} V={V}"
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_sweep_kv_append(sv, i):
+    """The paged KV append on seeded batches (1-24 requests, k = 0-15,
+    shuffled tables): the verify group's rows go to the positions just below
+    each request's length (crossing page boundaries), about 10% of the tokens
+    are skipped (-1); the pool must equal the oracle's bit for bit."""
+    rng = np.random.default_rng(6000 + i)
+    R = int(rng.integers(1, 25))
+    k = int(rng.integers(0, 16))
+    lens = tuple(int(x) for x in rng.integers(k + 1, 3000, size=R))
+    cfg = small_config("c0", R=R, k=k, H=8, kv_lens=lens, kv_len_range=None, shuffled=True, vocab=64)
+    inp = make_inputs(cfg, seed=6100 + i)
+    k1 = k + 1
+    pos = np.empty(R * k1, dtype=np.int32)
+    for r in range(R):
+        L = int(inp["kv_lens_in"][r])
+        pos[r * k1:(r + 1) * k1] = np.arange(L - k1, L)
+    pos[rng.random(pos.shape[0]) < 0.1] = -1
+    kv_new = rng.integers(0, 1 << 16, size=(R * k1, 512)).astype(np.uint16)
+    kv_new[(kv_new & 0x7F80) == 0x7F80] &= 0xBFFF  # no NaN / inf patterns among the random rows
+    ref = oracle.ref_kv_append(inp["kv_bits"], inp["block_table"], pos, kv_new, k1)
+    d = device_inputs(inp, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sv.mla_kv_append(bf16_tensor(kv_new, DEV), i32(pos, DEV), d["block_table"], d["kv"], k1, status=status)
+    torch.cuda.synchronize()
+    got = d["kv"].view(torch.int16).cpu().numpy().view(np.uint16)
+    assert int(status.item()) == 0
+    assert np.array_equal(got, ref), f"case {i}: R={R} k={k}"
