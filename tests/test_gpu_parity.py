@@ -215,6 +215,32 @@ def test_attention_longest_context(sv):
         check_attention(out, lse, ref_o, ref_l, label=f"131072 positions, splits={splits}, form={form}")
 
 
+@pytest.mark.parametrize("q_factor", [0.0, 16.0, 64.0])
+def test_attention_extreme_scores(sv, q_factor):
+    """A zero query (every visible row weighs the same: o is the mean of the
+    rows, lse = ln b) and a query scaled by 16 or 64 (scores spread over
+    hundreds of log2 units, so the running maximum moves again and again and
+    nearly all of each row's weight sits on a few KV rows), in every split
+    mode: the lazy rescale and the merge against the float64 oracle."""
+    cfg = small_config("c0", R=3, k=3, H=16, kv_lens=(2000, 700, 129), kv_len_range=None, shuffled=True,
+                       vocab=64)
+    inp = make_inputs(cfg, seed=17)
+    from workloads import f32_to_bf16_bits
+    q = inp["q_bits"].astype(np.uint32) << 16
+    q = f32_to_bf16_bits(q.view(np.float32) * np.float32(q_factor))
+    inp = dict(inp, q_bits=q)
+    ref_o, ref_l = oracle_attention(inp)
+    d = device_inputs(inp, DEV)
+    for splits in (1, 3, sv.SV_SPLITS_BALANCED):
+        for form in (sv.FORM_TWO_CTA, sv.FORM_STACKED):
+            status = torch.zeros(1, dtype=torch.int32, device=DEV)
+            out, lse = sv.mla_verify_decode(d["q"], d["kv"], d["block_table"], d["kv_bounds"], d["gate"], 4,
+                                            inp["softmax_scale"], num_splits=splits, status=status, form=form)
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+            check_attention(out, lse, ref_o, ref_l, label=f"q x {q_factor}, splits={splits}, form={form}")
+
+
 def test_attention_wave_mode(sv):
     """The wave split mode (the first k requests whole, the others in s
     pieces) on 30 requests x 3 row tiles x 2 halves = 180 CTAs: ragged
